@@ -1,0 +1,103 @@
+"""Pins of the oracle's GEMM entries and bias statistics: numpy's fp64 matrix
+product, the rotation-invariance of D = A B^T when both operands share the
+sign mask along K (and its failure when they do not), a hand-checkable case,
+and the hand-computed statistics fixture."""
+import os
+
+import numpy as np
+
+from fp4_microscaled_quantization_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def test_gemm_entries_match_library_product(orc):
+    rng = np.random.default_rng(0)
+    A = rng.standard_normal((40, 96)).astype(np.float32)
+    B = rng.standard_normal((24, 96)).astype(np.float32)
+    full = orc.gemm_ref(A, B, 0.5)
+    ii = rng.integers(0, 40, 300)
+    jj = rng.integers(0, 24, 300)
+    got = orc.gemm_entries(A, B, ii, jj, 0.5)
+    assert np.allclose(got, full[ii, jj], rtol=1e-12, atol=1e-12)
+    assert np.allclose(full, 0.5 * (A.astype(np.float64) @ B.astype(np.float64).T), rtol=1e-13)
+
+
+def _rotate_rows(orc, M, n_h, mask):
+    out = M.copy()
+    for r in range(M.shape[0]):
+        for c0 in range(0, M.shape[1], n_h):
+            out[r, c0:c0 + n_h] = orc.rotate_block(M[r, c0:c0 + n_h], n_h, mask)
+    return out
+
+
+def test_rotation_invariance_needs_shared_mask(orc):
+    rng = np.random.default_rng(1)
+    A = rng.standard_normal((16, 64)).astype(np.float32)
+    B = rng.standard_normal((8, 64)).astype(np.float32)
+    D = orc.gemm_ref(A, B)
+    for n_h in (16, 32):
+        mk = orc.sign_mask_from_seed(5, n_h)
+        Dr = orc.gemm_ref(_rotate_rows(orc, A, n_h, mk), _rotate_rows(orc, B, n_h, mk))
+        assert np.abs(Dr - D).max() <= 1e-5 * np.abs(D).max()
+        mk2 = orc.sign_mask_from_seed(6, n_h)
+        Dbad = orc.gemm_ref(_rotate_rows(orc, A, n_h, mk), _rotate_rows(orc, B, n_h, mk2))
+        assert np.abs(Dbad - D).max() > 0.1 * np.abs(D).max()
+
+
+def test_gemm_of_quantized_block_by_hand(orc):
+    """K = 32, one block per row: a = [6, 0, ...] at scale 2^0 and b = [1, 1, ...]
+    at scale 2^-2 (values 1 -> code for 4 at e = -2) gives D = 6 * 1 = 6."""
+    a = np.zeros((1, 32), np.float32)
+    a[0, 0] = 6.0
+    b = np.ones((1, 32), np.float32)
+    qa = orc.quantize(synth.to_bf16_bits(a), 0, 0, orc.SCALE_MX, 0)
+    qb = orc.quantize(synth.to_bf16_bits(b), 0, 0, orc.SCALE_MX, 0)
+    assert qa["scales"][0, 0] == 127 and qb["scales"][0, 0] == 125
+    da = orc.dequantize(qa["codes"], qa["scales"], 0, 0, orc.SCALE_MX)
+    db = orc.dequantize(qb["codes"], qb["scales"], 0, 0, orc.SCALE_MX)
+    assert orc.gemm_entries(da, db, [0], [0])[0] == 6.0
+
+
+def _golden_stats():
+    d = {}
+    for line in open(os.path.join(GOLDEN, "stats_example.txt")):
+        if line.strip() and not line.startswith("#"):
+            k, *v = line.split()
+            d[k] = [float(t) for t in v]
+    return d
+
+
+def test_stats_hand_example(orc):
+    g = _golden_stats()
+    s = orc.bias_stats(np.array(g["ref"], np.float32), np.array(g["approx"], np.float32))
+    assert abs(s["sqnr_db"] - g["sqnr_db"][0]) < 1e-12
+    assert abs(s["alpha"] - g["alpha"][0]) < 1e-15
+    assert abs(s["shrinkage"] - g["shrinkage"][0]) < 1e-15
+
+
+def test_stats_histogram_counts_codes(orc):
+    codes = np.array([0x10, 0x32, 0xFF], np.uint8)  # codes 0,1,2,3,15,15
+    s = orc.bias_stats(np.ones(6, np.float32), np.ones(6, np.float32), codes)
+    want = np.zeros(16, np.uint64)
+    for c in (0, 1, 2, 3, 15, 15):
+        want[c] += 1
+    assert np.array_equal(s["hist"], want)
+    assert s["sqnr_db"] == float("inf") and s["alpha"] == 1.0
+
+
+def test_e2m1_attenuates_more_than_e1m2_after_rotation(orc):
+    """Directional report (not a parity pin): on Gaussian data rotated by H16,
+    the E2M1 reconstruction shrinks magnitudes (alpha < 1) and E1M2 does not."""
+    x = synth.normal(128, 256, 31)
+    y = np.zeros((128, 256), np.float32)
+    for r in range(128):
+        for c0 in range(0, 256, 16):
+            y[r, c0:c0 + 16] = orc.rotate_block(synth.bf16_bits_to_f32(x[r, c0:c0 + 16]), 16, 0)
+    out = {}
+    for grid in (0, 1):
+        q = orc.quantize(x, 0, grid, orc.SCALE_MX, 16, 0)
+        d = orc.dequantize(q["codes"], q["scales"], 0, grid, orc.SCALE_MX)
+        out[grid] = orc.bias_stats(y, d)
+    print({g: (round(v["alpha"], 5), round(v["shrinkage"], 5), round(v["sqnr_db"], 3)) for g, v in out.items()})
+    assert out[0]["alpha"] < 1.0
