@@ -25,6 +25,7 @@
  * Readings of points the pages leave open are stated beside the step they
  * govern.
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -151,7 +152,8 @@ void orc_philox4x32_10(uint32_t out[4], const uint32_t ctr_in[4], const uint32_t
 }
 
 /* Rademacher sign mask D of the random Hadamard transform ([HTX] Experimento
- * de diagnostico: "Hadamard with random sign inversion"; [MX] Metodologia 3).
+ * de diagnostico: the randomized rotation flips signs at random before the
+ * Hadamard transform; [MX] Metodologia 3).
  * Reading: one n_h-bit mask per call and orientation, shared by every block;
  * bit j set negates element j of each block.  Drawn from Philox with
  * key = seed and counter (0, 0, 0x5349474E, 0); the low n_h bits of word 0. */
@@ -234,8 +236,8 @@ void orc_unrotate_block(float *u, int n, uint32_t sign_mask)
 /* Rounding onto the grid                                                   */
 /* ------------------------------------------------------------------------ */
 /* Round-to-nearest-even onto the grid ([SB] Declaracao do Problema and
- * Metodologia 2: RTNE for every operand but dY; [HTX] Que es MXFP4?: "the
- * value rounded to the nearest representable 4-bit number").
+ * Metodologia 2: RTNE for every operand but dY; [HTX] Que es MXFP4?: each
+ * element is the nearest value the 4-bit format can represent).
  * Magnitudes at or above q_max saturate to code 7.  An exact tie between
  * levels k and k+1 goes to the even code.  The sign bit is the sign of v, so
  * a negative value that rounds to zero keeps its sign (code 8). */
@@ -289,7 +291,8 @@ int orc_round_sr(int grid, float v, uint32_t r16)
  *
  *   grid      ORC_GRID_E2M1 or ORC_GRID_E1M2
  *   scale     ORC_SCALE_MX: b = 32, E8M0 shared exponent ([HTX] Que es MXFP4?)
- *             ORC_SCALE_NV: b = 16, E4M3 block scale, fp32 tensor scale
+ *             ORC_SCALE_NV: b = 16, E4M3 block scale, fp32 tensor scale,
+ *             v = y * fl(1 / (sb * S_t)) per element
  *   n_h       0 (no rotation), 16 or 32
  *   sign_mask bit j negates element j of every n_h block (0 = deterministic H)
  *   round     ORC_RTNE or ORC_SR (SR uses sr_seed and the stored index)
@@ -370,8 +373,7 @@ int orc_quantize(const uint16_t *x, int64_t R, int64_t C, int64_t ld, int orient
             }
 
             /* Step 5: scale.  v_t = y_t / scale. */
-            float vmul = 0.0f;   /* MX: exact power of two 2^-e */
-            float d = 0.0f;      /* NV: the dequantization step sb * S_t */
+            float vmul = 0.0f;   /* MX: exact power of two 2^-e; NV: 1 / (sb * S_t) */
             int zero_block = 0;
             uint8_t sbyte;
             if (scale == ORC_SCALE_MX) {
@@ -393,7 +395,11 @@ int orc_quantize(const uint16_t *x, int64_t R, int64_t C, int64_t ld, int orient
                 sbyte = (uint8_t)(e + 127);
                 vmul = ldexpf(1.0f, -e);
             } else {
-                /* E4M3 block scale = amax / q_max relative to S_t. */
+                /* E4M3 block scale = amax / q_max relative to S_t.
+                 * Reading: the pages only name NVFP4; the element step uses the
+                 * block's reciprocal dequantization step r = fl(1 / (sb * S_t))
+                 * (one division per block, v = fl(y * r)); an infinite r is
+                 * replaced by the largest finite float. */
                 if (S_t > 0.0f) {
                     float t1 = m / qmax;
                     float t2 = t1 / S_t;
@@ -401,8 +407,13 @@ int orc_quantize(const uint16_t *x, int64_t R, int64_t C, int64_t ld, int orient
                 } else {
                     sbyte = 0;
                 }
-                if (sbyte == 0) zero_block = 1;
-                else d = orc_e4m3_decode(sbyte) * S_t;
+                if (sbyte == 0) {
+                    zero_block = 1;
+                } else {
+                    float d = orc_e4m3_decode(sbyte) * S_t;
+                    vmul = 1.0f / d;
+                    if (isinf(vmul)) vmul = FLT_MAX;
+                }
             }
             scales[r * nblk + kb] = sbyte;
 
@@ -414,7 +425,7 @@ int orc_quantize(const uint16_t *x, int64_t R, int64_t C, int64_t ld, int orient
                 if (zero_block) {
                     code = signbit(blk[t]) ? 8 : 0;
                 } else {
-                    float v = (scale == ORC_SCALE_MX) ? blk[t] * vmul : blk[t] / d;
+                    float v = blk[t] * vmul;
                     if (round == ORC_SR)
                         code = orc_round_sr(grid, v, orc_sr_uniform16(sr_seed, (uint64_t)idx, (uint32_t)orient));
                     else
