@@ -1,0 +1,401 @@
+"""Benchmark of the fused Hadamard + FP4 quantizer and block-scaled FP4 GEMM.
+
+One step = the whole hot path for one linear layer of a Llama-3.1-8B-class
+model (synthetic, seeded): the fused rotation + MXFP4 quantization of X
+[16384, 4096], W [4096, 4096] and dY [16384, 4096], both orientations each,
+then the Fprop, Dgrad and Wgrad block-scaled GEMMs (E2M1 recipe: random H16
+with signs shared along each contraction axis, RTNE on X and W, SR on dY).
+
+  value        fused quantize throughput, GB/s of algorithmic bytes (read bf16,
+               write codes + scales of both copies) over the quantize phase
+  gemm.tflops  block-scaled GEMM throughput over the GEMM phase
+  e2e          the same two metrics through the C ABI from pinned host
+               buffers: inputs copied host->device inside the quantize phase,
+               GEMM outputs copied device->host inside the GEMM phase
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 run under torch.distributed.run: every rank runs the same per-rank
+workload on its own GPU (replicas, weak scaling); the time is the max over
+ranks and value counts the bytes of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+TOKENS, D_IN, D_OUT = 16384, 4096, 4096
+SEED = 1005
+MX_BYTES_PER_ELEM = 2 + 2 * (0.5 + 1 / 32)     # bf16 in, two copies of codes + E8M0 scales
+WORKLOAD = ("one linear layer, bf16 X[16384,4096] W[4096,4096] dY[16384,4096]: fused random-H16 + "
+            "MXFP4 E2M1 quantization of all three (row+col copies; RTNE X/W, Philox SR dY), then "
+            "Fprop Y=XW^T, Dgrad dX=dY W, Wgrad dW=dY^T X block-scaled FP4 GEMMs (bf16 out)")
+
+
+# ------------------------------------------------------------------ ranks
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def allreduce_max(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(bytes_per_rank: float, seconds_per_rank: float, world: int, device=None) -> float:
+    """Whole-job throughput: bytes of all ranks over the slowest rank's time."""
+    return bytes_per_rank * world / allreduce_max(seconds_per_rank, world, device)
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = bus_id
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.bus_id:
+            cmd += ["-i", self.bus_id]
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        rows = [l.split(",") for l in open(self.path) if l.strip()]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    from fp4_microscaled_quantization_gb300 import fp4q, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    bf16_peak = peaks.get("bf16_tflops", 1900.0)
+    fp4_peak = bf16_peak * (13.5 / 2.25)     # nominal dense FP4 : BF16 ratio on GB300
+    peak_src = "measured" if peaks else "fallback"
+
+    # ---------------- inputs (bf16, resident)
+    Xb, Wb, dYb = synth.layer(TOKENS, D_IN, D_OUT, SEED)
+    X, W, dY = (synth.as_torch(a).to(dev) for a in (Xb, Wb, dYb))
+    mK = fp4q.sign_mask_from_seed(SEED, 16)
+    mN = fp4q.sign_mask_from_seed(SEED + 1, 16)
+    mM = fp4q.sign_mask_from_seed(SEED + 2, 16)
+    cfg_x = fp4q.Config(grid=fp4q.GRID_E2M1, rot=16, sign_mask_row=mK, sign_mask_col=mM, sf_layout=fp4q.SF_MMA)
+    cfg_w = fp4q.Config(grid=fp4q.GRID_E2M1, rot=16, sign_mask_row=mK, sign_mask_col=mN, sf_layout=fp4q.SF_MMA)
+    cfg_g = fp4q.Config(grid=fp4q.GRID_E2M1, rot=16, sign_mask_row=mN, sign_mask_col=mM, round=fp4q.SR,
+                        sr_seed=SEED + 3, sf_layout=fp4q.SF_MMA)
+    Xr, Xc = fp4q.alloc_operand(TOKENS, D_IN, cfg_x, dev), fp4q.alloc_operand(D_IN, TOKENS, cfg_x, dev)
+    Wr, Wc = fp4q.alloc_operand(D_OUT, D_IN, cfg_w, dev), fp4q.alloc_operand(D_IN, D_OUT, cfg_w, dev)
+    Gr, Gc = fp4q.alloc_operand(TOKENS, D_OUT, cfg_g, dev), fp4q.alloc_operand(D_OUT, TOKENS, cfg_g, dev)
+    Y = torch.empty((TOKENS, D_OUT), dtype=torch.bfloat16, device=dev)
+    dX = torch.empty((TOKENS, D_IN), dtype=torch.bfloat16, device=dev)
+    dW = torch.empty((D_OUT, D_IN), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
+
+    q_bytes = MX_BYTES_PER_ELEM * (TOKENS * D_IN + D_OUT * D_IN + TOKENS * D_OUT)
+    flops = 3 * 2.0 * TOKENS * D_IN * D_OUT
+    launches_per_step = 6
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    kq = {"x": [], "w": [], "g": []}
+    kg = {"fprop": [], "dgrad": [], "wgrad": []}
+
+    def quantize_phase(rec=None):
+        e = [ev() for _ in range(4)] if rec is not None else None
+        if e: e[0].record(stream)
+        fp4q.rht_quantize(X, cfg_x, Xr, Xc, status=status, stream=stream)
+        if e: e[1].record(stream)
+        fp4q.rht_quantize(W, cfg_w, Wr, Wc, status=status, stream=stream)
+        if e: e[2].record(stream)
+        fp4q.rht_quantize(dY, cfg_g, Gr, Gc, status=status, stream=stream)
+        if e: e[3].record(stream)
+        if rec is not None:
+            rec.append(("q", e))
+
+    def gemm_phase(rec=None):
+        e = [ev() for _ in range(4)] if rec is not None else None
+        if e: e[0].record(stream)
+        fp4q.gemm(Xr, Wr, fp4q.GRID_E2M1, fp4q.SCALE_MX, want_f32=False, D_bf16=Y, status=status, stream=stream)
+        if e: e[1].record(stream)
+        fp4q.gemm(Gr, Wc, fp4q.GRID_E2M1, fp4q.SCALE_MX, want_f32=False, D_bf16=dX, status=status, stream=stream)
+        if e: e[2].record(stream)
+        fp4q.gemm(Gc, Xc, fp4q.GRID_E2M1, fp4q.SCALE_MX, want_f32=False, D_bf16=dW, status=status, stream=stream)
+        if e: e[3].record(stream)
+        if rec is not None:
+            rec.append(("g", e))
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        quantize_phase()
+        gemm_phase()
+    torch.cuda.synchronize(dev)
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item():#x} during warm-up")
+
+    bus = None
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+    except AttributeError:
+        pass
+    clocks = ClockSampler(bus)
+    clocks.start()
+    time.sleep(0.3)
+    recs = []
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        flush.zero_()        # outside the events: evict the previous step from L2
+        quantize_phase(recs)
+        gemm_phase(recs)
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item():#x} in the timed region")
+
+    q_times, g_times = [], []
+    for kind, e in recs:
+        per = [e[i].elapsed_time(e[i + 1]) * 1e-3 for i in range(3)]
+        (q_times if kind == "q" else g_times).append(sum(per))
+        for key, t in zip(("x", "w", "g") if kind == "q" else ("fprop", "dgrad", "wgrad"), per):
+            (kq if kind == "q" else kg)[key].append(t)
+    q_s = sum(q_times) / len(q_times)
+    g_s = sum(g_times) / len(g_times)
+    value = aggregate(q_bytes, q_s, world, dev) / 1e9
+    gemm_tflops = aggregate(flops, g_s, world, dev) / 1e12
+
+    # ---------------- end to end through the C ABI from pinned host buffers
+    hX, hW, hdY = (t.cpu().pin_memory() for t in (X, W, dY))
+    hY, hdX, hdW = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (Y, dX, dW))
+    h2d = sum(t.numel() * t.element_size() for t in (hX, hW, hdY))
+    d2h = sum(t.numel() * t.element_size() for t in (hY, hdX, hdW))
+    e2e_q, e2e_g = [], []
+    for it in range(args.warmup + args.steps):
+        flush.zero_()
+        e = [ev() for _ in range(3)]
+        e[0].record(stream)
+        X.copy_(hX, non_blocking=True)
+        W.copy_(hW, non_blocking=True)
+        dY.copy_(hdY, non_blocking=True)
+        quantize_phase()
+        e[1].record(stream)
+        gemm_phase()
+        hY.copy_(Y, non_blocking=True)
+        hdX.copy_(dX, non_blocking=True)
+        hdW.copy_(dW, non_blocking=True)
+        e[2].record(stream)
+        e[2].synchronize()
+        if it >= args.warmup:
+            e2e_q.append(e[0].elapsed_time(e[1]) * 1e-3)
+            e2e_g.append(e[1].elapsed_time(e[2]) * 1e-3)
+    e2e_value = aggregate(q_bytes, sum(e2e_q) / len(e2e_q), world, dev) / 1e9
+    e2e_gemm = aggregate(flops, sum(e2e_g) / len(e2e_g), world, dev) / 1e12
+
+    # ---------------- rooflines of the two kernels (per-launch averages)
+    g_launch = statistics.mean(kg["fprop"] + kg["dgrad"] + kg["wgrad"])
+    g_achieved = 2.0 * TOKENS * D_IN * D_OUT / g_launch / 1e12
+    x_launch = statistics.mean(kq["x"])
+    x_bytes = MX_BYTES_PER_ELEM * TOKENS * D_IN
+    x_achieved = x_bytes / x_launch / 1e9
+    traffic = json.load(open(os.path.join(ROOT, "profiles", "traffic.json"))) if os.path.exists(
+        os.path.join(ROOT, "profiles", "traffic.json")) else {}
+    dominant_gemm = sum(g_times) >= sum(q_times)
+    roof_gemm = {"kernel": "bs_gemm_kernel<mxf4> (tcgen05)", "bound": "tensor", "achieved": round(g_achieved, 1),
+                 "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(g_achieved / fp4_peak, 4),
+                 "traffic": traffic.get("gemm_mxf4_fprop_bytes"),
+                 "peak_source": f"{peak_src} bf16 burst x 6 (nominal FP4:BF16 dense ratio)"}
+    roof_q = {"kernel": "rht_quant_kernel (X, both copies)", "bound": "hbm", "achieved": round(x_achieved, 1),
+              "peak": hbm_peak, "unit": "GB/s", "frac": round(x_achieved / hbm_peak, 4),
+              "traffic": traffic.get("quant_x_bytes"), "peak_source": f"{peak_src} HBM copy"}
+
+    line = {
+        "metric": "fused RHT+FP4 quantize GB/s and % of HBM peak; block-scaled FP4 GEMM TFLOPS",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round((q_s + g_s) * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp4-e2m1 (fp32 quantizer arithmetic, fp32 accumulate)",
+        "data": "synthetic (seeded; shapes of Llama-3.1-8B hidden 4096, 16384 tokens)",
+        "config": {"workload": WORKLOAD, "global_batch_tokens": TOKENS * world, "per_rank": "replica",
+                   "l2": "flushed (256 MiB write) before every timed step", "recipe": "E2M1 MXFP4 H16"},
+        "hbm_frac": round(value / world / hbm_peak, 4),
+        "quantize": {"us_per_step": round(q_s * 1e6, 2), "gb_s": round(value, 1),
+                     "bytes_per_step": q_bytes, "per_tensor_us": {k: round(statistics.mean(v) * 1e6, 2)
+                                                                  for k, v in kq.items()}},
+        "gemm": {"tflops": round(gemm_tflops, 1), "us_per_step": round(g_s * 1e6, 2), "flops_per_step": flops,
+                 "per_gemm_us": {k: round(statistics.mean(v) * 1e6, 2) for k, v in kg.items()}},
+        "roofline": roof_gemm if dominant_gemm else roof_q,
+        "roofline_other": roof_q if dominant_gemm else roof_gemm,
+        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "gemm_tflops": round(e2e_gemm, 1),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "H2D of X/W/dY inside the quantize phase, D2H of Y/dX/dW inside the GEMM phase"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "wall_s_timed": round(wall, 4),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args)
+    return line
+
+
+# ------------------------------------------------------------------ oracle arm
+def _oracle_sample(rows: int):
+    from fp4_microscaled_quantization_gb300 import synth
+    Xb, Wb, dYb = synth.layer(TOKENS, D_IN, D_OUT, SEED)
+    return Xb[:rows].copy(), Wb[: max(128, rows // 4)].copy(), dYb[:rows].copy()
+
+
+def _oracle_step(orc, Xs, Ws, Gs, mK, mN, mM):
+    orc.quantize(Xs, 0, 0, 0, 16, mK)
+    orc.quantize(Xs, 1, 0, 0, 16, mM)
+    orc.quantize(Ws, 0, 0, 0, 16, mK)
+    orc.quantize(Ws, 1, 0, 0, 16, mN)
+    orc.quantize(Gs, 0, 0, 0, 16, mN, orc.SR, SEED + 3)
+    orc.quantize(Gs, 1, 0, 0, 16, mM, orc.SR, SEED + 3)
+
+
+def cpu_baseline(args, rows: int = 1024, min_s: float = 10.0) -> dict:
+    """The CPU oracle (single-threaded C) on a bounded sample of the same step."""
+    import oracle
+    orc = oracle
+    orc.build()
+    Xs, Ws, Gs = _oracle_sample(rows)
+    mK, mN, mM = (orc.sign_mask_from_seed(SEED + i, 16) for i in range(3))
+    nbytes = MX_BYTES_PER_ELEM * (Xs.size + Ws.size + Gs.size)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        _oracle_step(orc, Xs, Ws, Gs, mK, mN, mM)
+        n += 1
+        if time.perf_counter() - t0 >= min_s:
+            break
+    dt = (time.perf_counter() - t0) / n
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"quantize (both copies) of rows 0..{rows - 1} of X and dY and rows 0..{Ws.shape[0] - 1} "
+                      f"of W of the same workload, {n} repetitions, {dt:.2f} s each; GEMMs not included"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    rows = 256
+    Xs, Ws, Gs = _oracle_sample(rows)
+    mK, mN, mM = (oracle.sign_mask_from_seed(SEED + i, 16) for i in range(3))
+    nbytes = MX_BYTES_PER_ELEM * (Xs.size + Ws.size + Gs.size)
+    for _ in range(args.warmup):
+        _oracle_step(oracle, Xs, Ws, Gs, mK, mN, mM)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(oracle, Xs, Ws, Gs, mK, mN, mM)
+    dt = (time.perf_counter() - t0) / args.steps
+    v = round(nbytes / dt / 1e9, 4)
+    sample = (f"quantize (both copies) of rows 0..{rows - 1} of X and dY and rows 0..{Ws.shape[0] - 1} of W "
+              f"per step; GEMMs not included")
+    return {"impl": "reference", "metric": "fused RHT+FP4 quantize GB/s and % of HBM peak; block-scaled FP4 GEMM TFLOPS",
+            "value": v, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp32 quantizer arithmetic (CPU oracle)", "data": "synthetic (seeded)",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_ours(args, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
