@@ -118,3 +118,52 @@ cudaError_t launch_bias_stats(const StatsParams& sp, cudaStream_t s) {
 }
 
 }  // namespace fp4q
+
+// ------------------------------------------------------------------------
+// Allocation-free variant of the bias statistics.
+//
+// The reduction's scratch (per-CTA partial sums, histogram partials and the
+// arrival counter) lives in this file-scope device array instead of a caller
+// workspace, so a caller that may not allocate device memory can still run
+// it.  Every GPU that loads the library keeps the array until the process
+// exits.  Its device address is looked up once per device (the first call on
+// that device, with the device current) and cached; in host code the symbol is
+// only a host-side stand-in and must never be handed to a kernel directly.
+// All calls share the array: the counter is cleared on every call and the
+// partials are overwritten, but two calls that overlap on the GPU (different
+// streams, or different host threads) race on it.
+// ------------------------------------------------------------------------
+namespace {
+constexpr size_t kNoAllocScratchBytes = 128 * 1024;
+constexpr int kMaxDevices = 64;
+__device__ __align__(256) unsigned char g_stats_scratch[kNoAllocScratchBytes];
+void* g_scratch_addr[kMaxDevices] = {};
+}  // namespace
+
+extern "C" int32_t fp4q_bias_stats_noalloc(const float* ref, const float* approx, int64_t n,
+                                           const uint8_t* codes, void* out, void* stream) {
+  using namespace fp4q;
+  if (n < 0 || !out) return FP4Q_ERR_INVALID_ARG;
+  if (n > 0 && (!ref || !approx)) return FP4Q_ERR_INVALID_ARG;
+  if (codes && (n % 2 != 0)) return FP4Q_ERR_INVALID_ARG;
+  if (bias_stats_workspace(n) > kNoAllocScratchBytes) return FP4Q_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(out) % 8) != 0) return FP4Q_ERR_ALIGNMENT;
+  if (n > 0 && ((reinterpret_cast<uintptr_t>(ref) | reinterpret_cast<uintptr_t>(approx)) % 16) != 0)
+    return FP4Q_ERR_ALIGNMENT;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FP4Q_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FP4Q_ERR_UNSUPPORTED;
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_stats_scratch) != cudaSuccess || !p) return FP4Q_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  StatsParams sp;
+  sp.ref = ref;
+  sp.approx = approx;
+  sp.codes = codes;
+  sp.n = n;
+  sp.workspace = g_scratch_addr[dev];
+  sp.out = out;
+  return launch_bias_stats(sp, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+}

@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.fp4q_bias_stats_workspace_bytes.argtypes = [i64]
         L.fp4q_bias_stats.restype = i32
         L.fp4q_bias_stats.argtypes = [P, P, i64, P, P, sz, P, P]
+        L.fp4q_bias_stats_noalloc.restype = i32
+        L.fp4q_bias_stats_noalloc.argtypes = [P, P, i64, P, P, P]
         L.fp4q_stats_finalize.restype = None
         L.fp4q_stats_finalize.argtypes = [P, P, P, P]
         L.fp4q_hadamard_rotate_bf16.restype = i32

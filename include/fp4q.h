@@ -199,6 +199,26 @@ size_t fp4q_bias_stats_workspace_bytes(int64_t n);
 int32_t fp4q_bias_stats(const float* ref, const float* approx, int64_t n, const uint8_t* codes,
                         void* workspace, size_t ws_bytes, void* out, void* stream);
 
+/* Allocation-free form of fp4q_bias_stats.  The pages have no counterpart:
+ * this exists for callers that cannot allocate device memory -- a host
+ * framework or serving runtime that owns every device byte through its own
+ * pre-reserved pool, a plugin running inside another program's fixed memory
+ * budget, or a path that must not pay for cudaMalloc's implicit device
+ * synchronisation.  They still pass the inputs and the output buffer; the reduction's scratch is a 128 KiB device array
+ * built into the library (held on every GPU that loads it until the process
+ * exits).  Same arguments, results and determinism as fp4q_bias_stats.
+ *  - Calls whose scratch need (fp4q_bias_stats_workspace_bytes(n)) exceeds the
+ *    built-in 128 KiB return FP4Q_ERR_WORKSPACE; the current reduction needs
+ *    about 100 KiB for every n, so every n >= 0 fits.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - All calls share the one array: two calls that overlap on the GPU (other
+ *    streams, other host threads) race and give undefined sums.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine. */
+int32_t fp4q_bias_stats_noalloc(const float* ref, const float* approx, int64_t n, const uint8_t* codes,
+                                void* out, void* stream);
+
 /* Host helper: SQNR (dB), alpha and shrinkage from the five sums above. */
 void fp4q_stats_finalize(const double* sums5, double* sqnr_db, double* alpha, double* shrinkage);
 
