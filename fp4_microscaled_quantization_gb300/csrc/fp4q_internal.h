@@ -2,6 +2,7 @@
 // kernels of libfp4q.so (not part of the public ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -28,6 +29,11 @@ struct QuantParams {
   uint32_t sgn_row[32];  // bit 31 set: negate element t of a 32-element chunk (row-wise)
   uint32_t sgn_col[32];  // same, column-wise copy
 };
+
+// 2-D tensor map (inner dimension contiguous) and the device's SM count.
+bool encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t rows,
+                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw);
+int num_sms();
 
 struct DequantParams {
   const uint8_t* codes;

@@ -9,7 +9,8 @@
 //   E1M2 + MX                    -> kind::mxf8f6f4 on the E4M3 byte copies
 //                                   (every E1M2 level k/4 is exact in E4M3)
 //
-// Structure (one CTA per 128 x 256 output tile, 192 threads):
+// Structure (persistent, one CTA per SM walking 128 x 256 output tiles, 192
+// threads):
 //   warp 0      TMA producer: A/B tiles (128-byte swizzled K-major rows) by
 //               cp.async.bulk.tensor, scale-factor chunks by cp.async.bulk,
 //               into a 4-stage ring guarded by full/empty mbarriers.
@@ -17,7 +18,8 @@
 //               factors to TMEM (tcgen05.cp 32x128b.warpx4) and issues the
 //               MMAs, then tcgen05.commit frees the stage.
 //   warps 2-5   epilogue: TMEM -> registers (tcgen05.ld), alpha, bf16/fp32
-//               stores.
+//               stores; TMEM is released before the global stores so the
+//               next tile's MMAs overlap them.
 // Every mbarrier wait is bounded (about 2 s of %globaltimer); on expiry the
 // CTA raises FP4Q_DEV_TIMEOUT, stops issuing work, frees its TMEM and exits.
 #include <cuda.h>
@@ -28,6 +30,7 @@
 
 #include "../../include/fp4q.h"
 #include "fp4q_dev.cuh"
+#include "fp4q_internal.h"
 
 namespace fp4q {
 namespace {
@@ -166,6 +169,19 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint3
   }
 }
 
+// 32 consecutive fp32 accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 // Instruction descriptor of the block-scaled kinds: B scale id in bits 4-5,
 // A/B element types in 7-9 / 10-12, K-major A and B, N >> 3 in 17-22, scale
 // type in 23 (1 = E8M0, 0 = E4M3), M >> 4 in 24-28, A scale id in 29-30.
@@ -178,6 +194,13 @@ __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
 }
 
 // ------------------------------------------------------------ the kernel
+// Persistent: CTA b owns tiles b, b + G, b + 2G, ... (G = gridDim.x), tile id
+// -> (m block = id / n_blocks, n block = id % n_blocks).  The producer and
+// the MMA issuer stream through every (tile, K-tile) pair of the CTA without
+// draining the ring between tiles.  The accumulator is single-buffered: the
+// epilogue pulls a finished tile out of TMEM (as packed bf16 when only bf16 is
+// wanted), releases TMEM through acc_empty, and only then writes global
+// memory, so the next tile's MMAs overlap those stores.
 template <int KIND>
 __global__ void __launch_bounds__(NTHREADS, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -186,14 +209,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar_full = sbase + BAR_OFF;         // STAGES x 8 bytes
-  const uint32_t bar_empty = bar_full + 8 * STAGES;  // STAGES x 8 bytes
-  const uint32_t bar_acc = bar_empty + 8 * STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + BAR_OFF + 16 * STAGES + 8);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + BAR_OFF + 16 * STAGES + 16);
+  const uint32_t bar_full = sbase + BAR_OFF;          // STAGES x 8 bytes
+  const uint32_t bar_empty = bar_full + 8 * STAGES;   // STAGES x 8 bytes
+  const uint32_t bar_acc_full = bar_empty + 8 * STAGES;
+  const uint32_t bar_acc_empty = bar_acc_full + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + BAR_OFF + 16 * STAGES + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + BAR_OFF + 16 * STAGES + 24);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int n_blocks = (p.N + BN - 1) / BN;
+  const int n_tiles = (p.M / BM) * n_blocks;
   const int num_kt = (p.K + KK::kElemsPerTile - 1) / KK::kElemsPerTile;
   const int nq = p.K / KK::kBlock / 4;   // scale chunks per 128-row group
 
@@ -202,7 +227,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    mbar_init(bar_acc, 1);
+    mbar_init(bar_acc_full, 1);
+    mbar_init(bar_acc_empty, 4);   // one arrival per epilogue warp
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -222,128 +248,169 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // ---------------- producer
       asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
-      const bool rg1 = (n0 + 128) < p.N;
-      for (int kt = 0; kt < num_kt; ++kt) {
-        const int s = kt % STAGES;
-        const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
-        if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag)) {
-          *abort_flag = 1;
-          raise_status(p.status, FP4Q_DEV_TIMEOUT);
-          break;
+      uint32_t it = 0;
+      for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
+        const int m0 = (tile / n_blocks) * BM, n0 = (tile % n_blocks) * BN;
+        const bool rg1 = (n0 + 128) < p.N;
+        for (int kt = 0; kt < num_kt; ++kt, ++it) {
+          const int s = (int)(it % STAGES);
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag)) {
+            *abort_flag = 1;
+            raise_status(p.status, FP4Q_DEV_TIMEOUT);
+            break;
+          }
+          const int q0 = kt * KK::kChunksPerTile;
+          const int nch = min(KK::kChunksPerTile, nq - q0);
+          const uint32_t sf_bytes = (uint32_t)nch * 512u;
+          const uint32_t tx = A_BYTES + B_BYTES + sf_bytes * (rg1 ? 3u : 2u);
+          const uint32_t st = sbase + (uint32_t)s * STAGE_BYTES;
+          mbar_expect_tx(bar_full + 8 * s, tx);
+          tma_load_2d(st, &tmA, kt * KROW, m0, bar_full + 8 * s);
+          tma_load_2d(st + A_BYTES, &tmB, kt * KROW, n0, bar_full + 8 * s);
+          bulk_load(st + SFA_OFF, p.sfa + ((size_t)(m0 / 128) * nq + q0) * 512, sf_bytes, bar_full + 8 * s);
+          bulk_load(st + SFB_OFF, p.sfb + ((size_t)(n0 / 128) * nq + q0) * 512, sf_bytes, bar_full + 8 * s);
+          if (rg1)
+            bulk_load(st + SFB_OFF + KK::kChunksPerTile * 512, p.sfb + ((size_t)(n0 / 128 + 1) * nq + q0) * 512,
+                      sf_bytes, bar_full + 8 * s);
         }
-        const int q0 = kt * KK::kChunksPerTile;
-        const int nch = min(KK::kChunksPerTile, nq - q0);
-        const uint32_t sf_bytes = (uint32_t)nch * 512u;
-        const uint32_t tx = A_BYTES + B_BYTES + sf_bytes * (rg1 ? 3u : 2u);
-        const uint32_t st = sbase + (uint32_t)s * STAGE_BYTES;
-        mbar_expect_tx(bar_full + 8 * s, tx);
-        tma_load_2d(st, &tmA, kt * KROW, m0, bar_full + 8 * s);
-        tma_load_2d(st + A_BYTES, &tmB, kt * KROW, n0, bar_full + 8 * s);
-        bulk_load(st + SFA_OFF, p.sfa + ((size_t)(m0 / 128) * nq + q0) * 512, sf_bytes, bar_full + 8 * s);
-        bulk_load(st + SFB_OFF, p.sfb + ((size_t)(n0 / 128) * nq + q0) * 512, sf_bytes, bar_full + 8 * s);
-        if (rg1)
-          bulk_load(st + SFB_OFF + KK::kChunksPerTile * 512, p.sfb + ((size_t)(n0 / 128 + 1) * nq + q0) * 512,
-                    sf_bytes, bar_full + 8 * s);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      bool ok = true;
-      for (int kt = 0; kt < num_kt; ++kt) {
-        const int s = kt % STAGES;
-        const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
-        if (!mbar_wait(bar_full + 8 * s, ph, abort_flag)) {
+      uint32_t it = 0, tl = 0;
+      for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tl) {
+        if (!mbar_wait(bar_acc_empty, (tl & 1u) ^ 1u, abort_flag)) {
           *abort_flag = 1;
           raise_status(p.status, FP4Q_DEV_TIMEOUT);
-          ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t st = sbase + (uint32_t)s * STAGE_BYTES;
-        const uint32_t sfa_col = tmem + SF_COL0 + SF_COLS_PER_STAGE * (uint32_t)s;
-        const uint32_t sfb_col = sfa_col + 16;
-        const int q0 = kt * KK::kChunksPerTile;
-        const int nch = min(KK::kChunksPerTile, nq - q0);
-        for (int c = 0; c < nch; ++c) {
-          tc_cp_sf(sfa_col + 4 * c, sf_desc(st + SFA_OFF + 512 * c));
-          tc_cp_sf(sfb_col + 8 * c, sf_desc(st + SFB_OFF + 512 * c));
-          tc_cp_sf(sfb_col + 8 * c + 4, sf_desc(st + SFB_OFF + KK::kChunksPerTile * 512 + 512 * c));
-        }
-        const int rem = p.K - kt * KK::kElemsPerTile;
-        const int n_mma = min(4, rem / KK::kMmaK);
-        for (int k = 0; k < n_mma; ++k) {
-          uint32_t sfa = sfa_col, sfb = sfb_col, sf_id = 0;
-          if constexpr (KIND == KIND_MXF4) {
-            sfa += 4 * (k >> 1);
-            sfb += 8 * (k >> 1);
-            sf_id = 2u * (uint32_t)(k & 1);
-          } else if constexpr (KIND == KIND_NVF4) {
-            sfa += 4 * k;
-            sfb += 8 * k;
-          } else {
-            sf_id = (uint32_t)k;
+        bool ok = true;
+        for (int kt = 0; kt < num_kt; ++kt, ++it) {
+          const int s = (int)(it % STAGES);
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!mbar_wait(bar_full + 8 * s, ph, abort_flag)) {
+            *abort_flag = 1;
+            raise_status(p.status, FP4Q_DEV_TIMEOUT);
+            ok = false;
+            break;
           }
-          tc_mma<KIND>(tmem + ACC_COL, op_desc(st + 32 * k), op_desc(st + A_BYTES + 32 * k),
-                       make_idesc<KIND>(sf_id), sfa, sfb, (kt > 0 || k > 0) ? 1u : 0u);
+          tc_fence_after();
+          const uint32_t st = sbase + (uint32_t)s * STAGE_BYTES;
+          const uint32_t sfa_col = tmem + SF_COL0 + SF_COLS_PER_STAGE * (uint32_t)s;
+          const uint32_t sfb_col = sfa_col + 16;
+          const int q0 = kt * KK::kChunksPerTile;
+          const int nch = min(KK::kChunksPerTile, nq - q0);
+          for (int c = 0; c < nch; ++c) {
+            tc_cp_sf(sfa_col + 4 * c, sf_desc(st + SFA_OFF + 512 * c));
+            tc_cp_sf(sfb_col + 8 * c, sf_desc(st + SFB_OFF + 512 * c));
+            tc_cp_sf(sfb_col + 8 * c + 4, sf_desc(st + SFB_OFF + KK::kChunksPerTile * 512 + 512 * c));
+          }
+          const int rem = p.K - kt * KK::kElemsPerTile;
+          const int n_mma = min(4, rem / KK::kMmaK);
+          for (int k = 0; k < n_mma; ++k) {
+            uint32_t sfa = sfa_col, sfb = sfb_col, sf_id = 0;
+            if constexpr (KIND == KIND_MXF4) {
+              sfa += 4 * (k >> 1);
+              sfb += 8 * (k >> 1);
+              sf_id = 2u * (uint32_t)(k & 1);
+            } else if constexpr (KIND == KIND_NVF4) {
+              sfa += 4 * k;
+              sfb += 8 * k;
+            } else {
+              sf_id = (uint32_t)k;
+            }
+            tc_mma<KIND>(tmem + ACC_COL, op_desc(st + 32 * k), op_desc(st + A_BYTES + 32 * k),
+                         make_idesc<KIND>(sf_id), sfa, sfb, (kt > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(bar_empty + 8 * s);
         }
-        tc_commit(bar_empty + 8 * s);
+        if (!ok) break;
+        tc_commit(bar_acc_full);
       }
-      if (ok) tc_commit(bar_acc);
     }
     __syncwarp();
   } else {
     // ---------------- epilogue (warps 2..5 -> TMEM lane quarters 2, 3, 0, 1)
     const int sp = warp & 3;
-    const int row = m0 + 32 * sp + lane;
-    bool ok = mbar_wait(bar_acc, 0u, abort_flag);
-    if (!ok) {
-      *abort_flag = 1;
-      raise_status(p.status, FP4Q_DEV_TIMEOUT);
-    }
-    ok = __all_sync(0xFFFFFFFFu, ok);
-    tc_fence_after();
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * sp) << 16) + ACC_COL;
     float alpha = 1.0f;
     if constexpr (KIND == KIND_NVF4) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
-    if (ok) {
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        if (n0 + c0 >= p.N) break;
-        uint32_t r[32];
-        const uint32_t taddr = tmem + ((uint32_t)(32 * sp) << 16) + ACC_COL + (uint32_t)c0;
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-            "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-              "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
-              "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
-              "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-            : "r"(taddr));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        float v[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          v[j] = __uint_as_float(r[j]);
-          if constexpr (KIND == KIND_NVF4) v[j] = __fmul_rn(v[j], alpha);
+    uint32_t tl = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tl) {
+      const int m0 = (tile / n_blocks) * BM, n0 = (tile % n_blocks) * BN;
+      const int row = m0 + 32 * sp + lane;
+      bool ok = mbar_wait(bar_acc_full, tl & 1u, abort_flag);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          raise_status(p.status, FP4Q_DEV_TIMEOUT);
         }
-        const size_t off = (size_t)row * p.N + n0 + c0;
-        if (p.d_f32) {
-          float4* dst = reinterpret_cast<float4*>(p.d_f32 + off);
+        break;
+      }
+      tc_fence_after();
+      const int ncols = min(BN, p.N - n0);   // a multiple of 128
+      if (p.d_f32 == nullptr) {
+        // bf16 only: whole row to registers, release TMEM, then store
+        uint32_t h[BN / 2];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        }
-        if (p.d_bf16) {
-          uint32_t h[16];
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          if (c0 < ncols) {
+            uint32_t r[32];
+            tmem_ld32(lane_base + (uint32_t)c0, r);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-            h[j] = *reinterpret_cast<const uint32_t*>(&b2);
+            for (int j = 0; j < 16; ++j) {
+              float a = __uint_as_float(r[2 * j]), b = __uint_as_float(r[2 * j + 1]);
+              if constexpr (KIND == KIND_NVF4) {
+                a = __fmul_rn(a, alpha);
+                b = __fmul_rn(b, alpha);
+              }
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(a, b);
+              h[c0 / 2 + j] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
           }
-          uint4* dst = reinterpret_cast<uint4*>(p.d_bf16 + off);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_acc_empty) : "memory");
+        uint4* dst = reinterpret_cast<uint4*>(p.d_bf16 + (size_t)row * p.N + n0);
+#pragma unroll
+        for (int j = 0; j < BN / 8; ++j)
+          if (8 * j < ncols) dst[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+      } else {
+        // fp32 (and optional bf16): chunk by chunk, TMEM released at the end
+        for (int c0 = 0; c0 < ncols; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(lane_base + (uint32_t)c0, r);
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            v[j] = __uint_as_float(r[j]);
+            if constexpr (KIND == KIND_NVF4) v[j] = __fmul_rn(v[j], alpha);
+          }
+          const size_t off = (size_t)row * p.N + n0 + c0;
+          float4* df = reinterpret_cast<float4*>(p.d_f32 + off);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) df[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          if (p.d_bf16) {
+            uint32_t hb[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+              hb[j] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            uint4* db = reinterpret_cast<uint4*>(p.d_bf16 + off);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) db[j] = make_uint4(hb[4 * j], hb[4 * j + 1], hb[4 * j + 2], hb[4 * j + 3]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_acc_empty) : "memory");
       }
     }
   }
@@ -356,34 +423,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 // ------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  }
-  return fn;
-}
-
 // 2-D byte tensor [rows][row_bytes], box = 128 bytes x box_rows, 128B swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {row_bytes, rows};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {(cuuint32_t)KROW, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, (uint32_t)KROW,
+                        box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int KIND>
@@ -394,8 +437,9 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmPa
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const dim3 grid((unsigned)((p.N + BN - 1) / BN), (unsigned)(p.M / BM), 1);
-  bs_gemm_kernel<KIND><<<grid, NTHREADS, SMEM_BYTES, s>>>(a, b, p);
+  const int tiles = (p.M / BM) * ((p.N + BN - 1) / BN);
+  const int g = tiles < num_sms() ? tiles : num_sms();
+  bs_gemm_kernel<KIND><<<g, NTHREADS, SMEM_BYTES, s>>>(a, b, p);
   return cudaGetLastError();
 }
 

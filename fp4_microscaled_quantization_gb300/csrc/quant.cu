@@ -13,10 +13,11 @@
 //         E8M0 shared exponent, nearest 4-bit value).
 //
 // Design (GB300-first, HBM-bound):
-//   * One CTA owns a 64 x 256 bf16 tile (32 KB), read once from HBM with
-//     coalesced 16-byte loads into a bank-swizzled shared-memory tile.  Both
-//     the row-wise copy (blocks along columns) and the column-wise copy (blocks
-//     along rows, stored transposed) are produced from that one read.
+//   * Persistent CTAs (two per SM) walk 64 x 256 bf16 tiles (32 KB).  Each
+//     tile is read once from HBM by TMA into a 3-stage shared-memory ring
+//     (128-byte swizzle), so two tiles are in flight while one is computed.
+//     Both the row-wise copy (blocks along columns) and the column-wise copy
+//     (blocks along rows, stored transposed) come from that one read.
 //   * A "chunk" is 32 consecutive elements of one row or one column.  A thread
 //     holds a chunk as 16 fp32 pairs P[i] = (u[i], u[i+16]) so that every
 //     butterfly stage of stride < 16 is one packed FADD2/FFMA2 over two
@@ -38,12 +39,6 @@ namespace fp4q {
 constexpr int kTR = 64;    // tile rows
 constexpr int kTC = 256;   // tile columns
 constexpr int kNT = 256;   // threads per CTA
-constexpr int kUnitsPerRow = kTC * 2 / 16;  // 16-byte units per tile row (32)
-
-// 16-byte unit u of a tile row is stored at u ^ ((u >> 3) & 3): row-wise chunk
-// reads (8 threads on 8 chunks of one row) and column-pair reads (32 threads
-// on one 128-byte span) are both free of bank conflicts.
-__device__ __forceinline__ int swz(int u) { return u ^ ((u >> 3) & 3); }
 
 template <int GRID>
 struct GridK;
@@ -69,31 +64,37 @@ __device__ __forceinline__ uint32_t rtne_e1m2(float v) {
   return (__float_as_uint(t) & 7u) | ((__float_as_uint(v) >> 28) & 8u);
 }
 
-// SR onto {k/4}: s = 4|v| (exact), k0 = floor(s) by a round-down add of 2^23,
-// frac = s - k0 (exact); up iff r16 < frac * 2^16.
-__device__ __forceinline__ uint32_t sr_e1m2(float v, uint32_t r16) {
-  const float s = fminf(fabsf(v), 1.75f) * 4.0f;
-  float t;
+// Exact stochastic-rounding decision shared by both grids.  With s >= 0 the
+// position on a unit-spaced grid (s < 8), t = fl_rm(s + 2^23) holds floor(s) in
+// its low bits; C = 2^23 - floor(s) 2^16 is exact; y = fl_ru(s 2^16 + C) =
+// 2^23 + ceil(frac(s) 2^16); and r16 < frac(s) 2^16 (the rule r / 2^16 < f)
+// holds iff 2^23 + r16 < y.  Returns floor(s) + up.
+__device__ __forceinline__ uint32_t sr_unit(float s, float r_as_float) {
+  float t, y;
   asm("add.rm.f32 %0, %1, %2;" : "=f"(t) : "f"(s), "f"(8388608.0f));
-  const float fl = t - 8388608.0f;
-  const float frac = s - fl;
-  const uint32_t up = ((float)r16 < frac * 65536.0f) ? 1u : 0u;
-  return ((__float_as_uint(t) & 7u) + up) | ((__float_as_uint(v) >> 28) & 8u);
+  const float C = __fmaf_rn(t, -65536.0f, 549764202496.0f);   // 2^39 + 2^23 - t 2^16
+  asm("fma.rp.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(s), "f"(65536.0f), "f"(C));
+  return (__float_as_uint(t) & 7u) + ((r_as_float < y) ? 1u : 0u);
+}
+
+// 2^23 + r as a float, r the 16-bit uniform numerator (exact).
+__device__ __forceinline__ float r16_float(uint32_t r16) { return __uint_as_float(0x4B000000u | r16); }
+
+// SR onto {k/4}: s = 4 min(|v|, 1.75) is exact and lies on the unit grid.
+__device__ __forceinline__ uint32_t sr_e1m2(float v, float rf) {
+  const float s = fminf(fabsf(v), 1.75f) * 4.0f;
+  return sr_unit(s, rf) | ((__float_as_uint(v) >> 28) & 8u);
 }
 
 // SR onto E2M1: with E = clamp(floor(log2 |v|), 0, 2) the levels around |v|
-// are 2^(E-1) apart, s = |v| 2^(1-E) is exact, the lower level's code is
-// 2E + floor(s) and frac(s) is the distance to it in gaps.
-__device__ __forceinline__ uint32_t sr_e2m1(float v, uint32_t r16) {
+// are 2^(E-1) apart, s = |v| 2^(1-E) is exact, and the lower level's code is
+// 2E + floor(s) (floor(s) = 0..3 for E = 0, 2..3 above).
+__device__ __forceinline__ uint32_t sr_e2m1(float v, float rf) {
   const float a = fminf(fabsf(v), 6.0f);
-  int E = (int)(__float_as_uint(a) >> 23) - 127;
-  E = E < 0 ? 0 : (E > 2 ? 2 : E);
-  const float s = a * __uint_as_float((uint32_t)(128 - E) << 23);  // 2^(1-E)
-  float t;
-  asm("add.rm.f32 %0, %1, %2;" : "=f"(t) : "f"(s), "f"(8388608.0f));
-  const float frac = s - (t - 8388608.0f);
-  const uint32_t up = ((float)r16 < frac * 65536.0f) ? 1u : 0u;
-  return ((uint32_t)(2 * E) + (__float_as_uint(t) & 3u) + up) | ((__float_as_uint(v) >> 28) & 8u);
+  const uint32_t eb = __float_as_uint(fmaxf(a, 1.0f)) & 0x7F800000u;   // (127 + E) << 23
+  const float s = a * __uint_as_float(0x7F800000u - eb);              // 2^(1-E), exponent 128 - E
+  const uint32_t twoE = (eb >> 22) - 254u;
+  return (twoE + sr_unit(s, rf)) | ((__float_as_uint(v) >> 28) & 8u);
 }
 
 // E4M3 bytes of eight packed codes (element 0 in the low nibble): magnitude by
@@ -224,8 +225,8 @@ __device__ __forceinline__ void quantize_chunk(float2 (&P)[16], float S_t, uint6
       for (int j = 0; j < 8; ++j) {
         const int t = q * 8 + j;
         const float v = (t < 16) ? P[t].x : P[t - 16].y;
-        const uint32_t r16 = (j & 1) ? (r.v[j >> 1] >> 16) : (r.v[j >> 1] & 0xFFFFu);
-        const uint32_t code = (GRID == FP4Q_GRID_E1M2) ? sr_e1m2(v, r16) : sr_e2m1(v, r16);
+        const float rf = r16_float((j & 1) ? (r.v[j >> 1] >> 16) : (r.v[j >> 1] & 0xFFFFu));
+        const uint32_t code = (GRID == FP4Q_GRID_E1M2) ? sr_e1m2(v, rf) : sr_e2m1(v, rf);
         w |= code << (4 * j);
       }
       o.w[q] = w;
@@ -264,29 +265,60 @@ __device__ __forceinline__ void store_chunk(const CopyOut& d, int64_t r, int64_t
   }
 }
 
-// ------------------------------------------------------------ tile loading
-// Load the kTR x kTC tile at (tr0, tc0) into shared memory; rows or 8-column
-// units outside the matrix read as zero.
-__device__ __forceinline__ void load_tile(uint4* tile, const uint16_t* __restrict__ x, int64_t rows,
-                                          int64_t cols, int64_t ld, int64_t tr0, int64_t tc0) {
-#pragma unroll
-  for (int k = 0; k < (kTR * kUnitsPerRow) / kNT; ++k) {
-    const int id = threadIdx.x + kNT * k;
-    const int r = id / kUnitsPerRow, u = id % kUnitsPerRow;
-    const int64_t gr = tr0 + r, gc = tc0 + (int64_t)u * 8;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (gr < rows && gc < cols) v = __ldcs(reinterpret_cast<const uint4*>(x + gr * ld + gc));
-    tile[r * kUnitsPerRow + swz(u)] = v;
+// ------------------------------------------------------------ tile pipeline
+// Tiles of kTR x kTC bf16 arrive by TMA as four 64-row x 64-column boxes with
+// the 128-byte swizzle: within box b, logical row r occupies bytes
+// [r*128, r*128+128) and its 16-byte unit c sits at unit c ^ (r & 7).  The
+// thread <-> data mappings below keep both access patterns conflict-free:
+// eight threads of a quarter-warp read eight different rows of one row-wise
+// chunk (distinct r & 7), and a warp reads 32 consecutive words of one row.
+constexpr int kStages = 3;                       // tiles in flight per CTA
+constexpr int kTileBytes = kTR * kTC * 2;        // 32 KB
+constexpr int kQuantSmem = kStages * kTileBytes + 1024 + 64;
+
+struct TileView {
+  const uint8_t* t;
+  // 16-byte unit u (0..31) of logical tile row r
+  __device__ __forceinline__ uint4 unit(int r, int u) const {
+    return *reinterpret_cast<const uint4*>(t + ((u >> 3) << 13) + (r << 7) + (((u & 7) ^ (r & 7)) << 4));
+  }
+  // word holding columns 2p, 2p+1 of tile row r (p = 0..127)
+  __device__ __forceinline__ uint32_t word(int r, int p) const {
+    return *reinterpret_cast<const uint32_t*>(t + ((p >> 5) << 13) + (r << 7) +
+                                              ((((p >> 2) & 7) ^ (r & 7)) << 4) + ((p & 3) << 2));
+  }
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ bool mbar_done(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+               : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Wait for a phase of an mbarrier, giving up after about 2 s.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_done(bar, parity)) return true;
+    if ((i & 255u) == 255u) {
+      uint64_t now;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > 2000000000ull) return false;
+    }
   }
 }
 
-// Chunk of tile row r, 32-column chunk q (0..7), as pairs with signs applied.
-__device__ __forceinline__ void read_row_chunk(const uint4* tile, int r, int q, const uint32_t* sgn,
+// Row-wise chunk q (0..7) of tile row r as pairs with the signs applied.
+__device__ __forceinline__ void read_row_chunk(const TileView& tv, int r, int q, const uint32_t* sgn,
                                                float2 (&P)[16]) {
   uint32_t w[16];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const uint4 v = tile[r * kUnitsPerRow + swz(4 * q + j)];
+    const uint4 v = tv.unit(r, 4 * q + j);
     w[4 * j + 0] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
   }
   // word k holds elements 2k (low half) and 2k+1 (high half)
@@ -299,121 +331,181 @@ __device__ __forceinline__ void read_row_chunk(const uint4* tile, int r, int q, 
   }
 }
 
-// Word (bf16 pair of columns 2p, 2p+1) of tile row r.
-__device__ __forceinline__ uint32_t tile_word(const uint4* tile, int r, int p) {
-  const uint32_t* row = reinterpret_cast<const uint32_t*>(tile + r * kUnitsPerRow);
-  return row[swz(p >> 2) * 4 + (p & 3)];
+// Row-wise task g (0..511) of a tile -> (row, chunk): eight consecutive tasks
+// are eight rows with distinct r & 7 of one chunk.
+__device__ __forceinline__ void row_task(int g, int& r, int& q) {
+  r = (g & 7) | ((g >> 6) << 3);
+  q = (g >> 3) & 7;
+}
+
+// Persistent loop over the tiles of the matrix: CTA b takes tiles b, b + G,
+// b + 2G, ... (G = gridDim.x, column tiles fastest).  Thread 0 keeps kStages
+// TMA tile loads in flight; all threads wait on the tile's mbarrier, run
+// f(tile, tr0, tc0) and meet at a barrier before the stage is refilled.
+// Returns false (after raising FP4Q_DEV_TIMEOUT and draining its own loads)
+// when a load did not arrive within the bounded wait.
+template <class F>
+__device__ __forceinline__ bool tile_loop(const CUtensorMap* tm, int64_t rows, int64_t cols, uint32_t* status,
+                                          F&& f) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t bar0 = smem_addr(smem + kStages * kTileBytes);
+  const int ntc = (int)((cols + kTC - 1) / kTC);
+  const int ntiles = ntc * (int)((rows + kTR - 1) / kTR);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8 * s) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  auto issue = [&](int s, int tile) {
+    const int tr0 = (tile / ntc) * kTR, tc0 = (tile % ntc) * kTC;
+    const uint32_t bar = bar0 + 8 * s;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kTileBytes) : "memory");
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+          ::"r"(smem_addr(smem + s * kTileBytes + b * 8192)), "l"(tm), "r"(tc0 + 64 * b), "r"(tr0), "r"(bar)
+          : "memory");
+  };
+  if (threadIdx.x == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
+    for (int s = 0; s < kStages; ++s) {
+      const int t = blockIdx.x + s * gridDim.x;
+      if (t < ntiles) issue(s, t);
+    }
+  }
+  int k = 0;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+    const int s = k % kStages;
+    const bool ok = mbar_wait_bounded(bar0 + 8 * s, (uint32_t)(k / kStages) & 1u);
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) {
+        raise_status(status, FP4Q_DEV_TIMEOUT);
+        for (int j = 0; j < kStages; ++j) {   // bounded drain of this CTA's own loads
+          const int kk = k + j, tt = blockIdx.x + kk * gridDim.x;
+          if (tt < ntiles) (void)mbar_wait_bounded(bar0 + 8 * (kk % kStages), (uint32_t)(kk / kStages) & 1u);
+        }
+      }
+      __syncthreads();
+      return false;
+    }
+    f(TileView{smem + s * kTileBytes}, (int64_t)(tile / ntc) * kTR, (int64_t)(tile % ntc) * kTC);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int nt = tile + kStages * gridDim.x;
+      if (nt < ntiles) issue(s, nt);
+    }
+  }
+  return true;
 }
 
 // ------------------------------------------------------------ fused kernel
 template <int GRID, int SCALE, int NH, int ROUND>
-__global__ void __launch_bounds__(kNT, 2) rht_quant_kernel(const QuantParams p) {
-  __shared__ uint4 tile[kTR * kUnitsPerRow];
-  const int64_t tr0 = (int64_t)blockIdx.y * kTR, tc0 = (int64_t)blockIdx.x * kTC;
-  load_tile(tile, p.x, p.rows, p.cols, p.ld, tr0, tc0);
-  __syncthreads();
-
+__global__ void __launch_bounds__(kNT, 2)
+    rht_quant_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
   const uint32_t key0 = (uint32_t)p.sr_seed, key1 = (uint32_t)(p.sr_seed >> 32);
   constexpr float kDen = 448.0f * GridK<GRID>::kQmax;
-
-  // column-wise copy: thread owns columns 2cp, 2cp+1 of rows 32h .. 32h+31
-  if (p.want_col) {
-    float S_t = 0.0f;
-    if constexpr (SCALE == FP4Q_SCALE_NV) {
-      S_t = __fdiv_rn(p.gamax[1], kDen);
-      if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.col.tensor_scale = S_t;
+  float S_row = 0.0f, S_col = 0.0f;
+  if constexpr (SCALE == FP4Q_SCALE_NV) {
+    if (p.want_row) S_row = __fdiv_rn(p.gamax[0], kDen);
+    if (p.want_col) S_col = __fdiv_rn(p.gamax[1], kDen);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      if (p.want_row) *p.row.tensor_scale = S_row;
+      if (p.want_col) *p.col.tensor_scale = S_col;
     }
-    const int cp = threadIdx.x & 127, h = threadIdx.x >> 7;
-    const int64_t col = tc0 + 2 * cp, row0 = tr0 + 32 * h;
-    if (col < p.cols && row0 < p.rows) {
-      uint32_t w[32];
+  }
+  tile_loop(&tmx, p.rows, p.cols, p.status, [&](const TileView& tv, int64_t tr0, int64_t tc0) {
+    // column-wise copy: thread owns columns 2cp, 2cp+1 of tile rows 32h .. 32h+31
+    if (p.want_col) {
+      const int cp = threadIdx.x & 127, h = threadIdx.x >> 7;
+      const int64_t col = tc0 + 2 * cp, row0 = tr0 + 32 * h;
+      if (col < p.cols && row0 < p.rows) {
+        uint32_t w[32];
 #pragma unroll
-      for (int t = 0; t < 32; ++t) w[t] = tile_word(tile, 32 * h + t, cp);
+        for (int t = 0; t < 32; ++t) w[t] = tv.word(32 * h + t, cp);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float2 P[16];
+        for (int half = 0; half < 2; ++half) {
+          float2 P[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint32_t a = half ? (w[i] & 0xFFFF0000u) : (w[i] << 16);
-          const uint32_t b = half ? (w[i + 16] & 0xFFFF0000u) : (w[i + 16] << 16);
-          P[i].x = __uint_as_float(a ^ p.sgn_col[i]);
-          P[i].y = __uint_as_float(b ^ p.sgn_col[i + 16]);
+          for (int i = 0; i < 16; ++i) {
+            const uint32_t a = half ? (w[i] & 0xFFFF0000u) : (w[i] << 16);
+            const uint32_t b = half ? (w[i + 16] & 0xFFFF0000u) : (w[i + 16] << 16);
+            P[i].x = __uint_as_float(a ^ p.sgn_col[i]);
+            P[i].y = __uint_as_float(b ^ p.sgn_col[i + 16]);
+          }
+          rotate_chunk<NH>(P);
+          const int64_t c = col + half;
+          ChunkOut o;
+          quantize_chunk<GRID, SCALE, ROUND>(P, S_col, (uint64_t)(c * p.rows + row0), 1u, key0, key1,
+                                             p.emit_e4m3, p.status, o);
+          store_chunk<SCALE>(p.col, c, row0, p.rows, p.sf_mma, p.emit_e4m3, o);
         }
-        rotate_chunk<NH>(P);
-        const int64_t c = col + half;
-        ChunkOut o;
-        quantize_chunk<GRID, SCALE, ROUND>(P, S_t, (uint64_t)(c * p.rows + row0), 1u, key0, key1,
-                                           p.emit_e4m3, p.status, o);
-        store_chunk<SCALE>(p.col, c, row0, p.rows, p.sf_mma, p.emit_e4m3, o);
       }
     }
-  }
-
-  // row-wise copy: tasks (row r, chunk q), 8 consecutive threads per row
-  if (p.want_row) {
-    float S_t = 0.0f;
-    if constexpr (SCALE == FP4Q_SCALE_NV) {
-      S_t = __fdiv_rn(p.gamax[0], kDen);
-      if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.row.tensor_scale = S_t;
-    }
+    // row-wise copy: two (row, chunk) tasks per thread
+    if (p.want_row) {
 #pragma unroll 1
-    for (int k = 0; k < (kTR * (kTC / 32)) / kNT; ++k) {
-      const int id = threadIdx.x + kNT * k;
-      const int r = id >> 3, q = id & 7;
-      const int64_t gr = tr0 + r, gc = tc0 + 32 * q;
-      if (gr < p.rows && gc < p.cols) {
-        float2 P[16];
-        read_row_chunk(tile, r, q, p.sgn_row, P);
-        rotate_chunk<NH>(P);
-        ChunkOut o;
-        quantize_chunk<GRID, SCALE, ROUND>(P, S_t, (uint64_t)(gr * p.cols + gc), 0u, key0, key1,
-                                           p.emit_e4m3, p.status, o);
-        store_chunk<SCALE>(p.row, gr, gc, p.cols, p.sf_mma, p.emit_e4m3, o);
+      for (int k = 0; k < (kTR * (kTC / 32)) / kNT; ++k) {
+        int r, q;
+        row_task(threadIdx.x + kNT * k, r, q);
+        const int64_t gr = tr0 + r, gc = tc0 + 32 * q;
+        if (gr < p.rows && gc < p.cols) {
+          float2 P[16];
+          read_row_chunk(tv, r, q, p.sgn_row, P);
+          rotate_chunk<NH>(P);
+          ChunkOut o;
+          quantize_chunk<GRID, SCALE, ROUND>(P, S_row, (uint64_t)(gr * p.cols + gc), 0u, key0, key1,
+                                             p.emit_e4m3, p.status, o);
+          store_chunk<SCALE>(p.row, gr, gc, p.cols, p.sf_mma, p.emit_e4m3, o);
+        }
       }
     }
-  }
+  });
 }
 
 // ------------------------------------------------------------ amax pass
 // G of the rotated row-wise and column-wise copies (NVFP4-style recipe):
-// per-CTA maxima, then one atomicMax on the float bits (non-negative floats
-// order like their bit patterns).  amax[0..1] must hold 0 beforehand.
+// per-thread maxima over all tiles of the CTA, a CTA reduction, then one
+// atomicMax on the float bits (non-negative floats order like their bit
+// patterns).  amax[0..1] must hold 0 beforehand.
 template <int NH>
-__global__ void __launch_bounds__(kNT) rotated_amax_kernel(const QuantParams p, float* amax) {
-  __shared__ uint4 tile[kTR * kUnitsPerRow];
+__global__ void __launch_bounds__(kNT, 2) rotated_amax_kernel(const __grid_constant__ CUtensorMap tmx,
+                                                              const QuantParams p, float* amax) {
   __shared__ float red[2][kNT / 32];
-  const int64_t tr0 = (int64_t)blockIdx.y * kTR, tc0 = (int64_t)blockIdx.x * kTC;
-  load_tile(tile, p.x, p.rows, p.cols, p.ld, tr0, tc0);
-  __syncthreads();
   float mrow = 0.0f, mcol = 0.0f;
-  if (p.want_col) {
-    const int cp = threadIdx.x & 127, h = threadIdx.x >> 7;
+  tile_loop(&tmx, p.rows, p.cols, p.status, [&](const TileView& tv, int64_t, int64_t) {
+    // zero-filled padding contributes |0| and cannot raise the maximum
+    if (p.want_col) {
+      const int cp = threadIdx.x & 127, h = threadIdx.x >> 7;
 #pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-      float2 P[16];
+      for (int half = 0; half < 2; ++half) {
+        float2 P[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t wa = tile_word(tile, 32 * h + i, cp), wb = tile_word(tile, 32 * h + i + 16, cp);
-        P[i].x = __uint_as_float((half ? (wa & 0xFFFF0000u) : (wa << 16)) ^ p.sgn_col[i]);
-        P[i].y = __uint_as_float((half ? (wb & 0xFFFF0000u) : (wb << 16)) ^ p.sgn_col[i + 16]);
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t wa = tv.word(32 * h + i, cp), wb = tv.word(32 * h + i + 16, cp);
+          P[i].x = __uint_as_float((half ? (wa & 0xFFFF0000u) : (wa << 16)) ^ p.sgn_col[i]);
+          P[i].y = __uint_as_float((half ? (wb & 0xFFFF0000u) : (wb << 16)) ^ p.sgn_col[i + 16]);
+        }
+        rotate_chunk<NH>(P);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) mcol = absmax_nan(mcol, absmax_nan(P[i].x, P[i].y));
       }
-      rotate_chunk<NH>(P);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) mcol = absmax_nan(mcol, absmax_nan(P[i].x, P[i].y));
     }
-  }
-  if (p.want_row) {
+    if (p.want_row) {
 #pragma unroll 1
-    for (int k = 0; k < (kTR * (kTC / 32)) / kNT; ++k) {
-      const int id = threadIdx.x + kNT * k;
-      float2 P[16];
-      read_row_chunk(tile, id >> 3, id & 7, p.sgn_row, P);
-      rotate_chunk<NH>(P);
+      for (int k = 0; k < (kTR * (kTC / 32)) / kNT; ++k) {
+        int r, q;
+        row_task(threadIdx.x + kNT * k, r, q);
+        float2 P[16];
+        read_row_chunk(tv, r, q, p.sgn_row, P);
+        rotate_chunk<NH>(P);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) mrow = absmax_nan(mrow, absmax_nan(P[i].x, P[i].y));
+        for (int i = 0; i < 16; ++i) mrow = absmax_nan(mrow, absmax_nan(P[i].x, P[i].y));
+      }
     }
-  }
-  // (zero-filled padding contributes |0| and cannot raise the maximum)
+  });
   mrow = fabsf(mrow);
   mcol = fabsf(mcol);
 #pragma unroll
@@ -507,103 +599,137 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantParams d) {
 // Rotation only, written back in bf16 (RNE): the first kernel of the unfused
 // rotate-then-quantize comparison.
 template <int NH>
-__global__ void __launch_bounds__(kNT) rotate_bf16_kernel(const QuantParams p, uint16_t* y_row, uint16_t* y_col) {
-  __shared__ uint4 tile[kTR * kUnitsPerRow];
-  const int64_t tr0 = (int64_t)blockIdx.y * kTR, tc0 = (int64_t)blockIdx.x * kTC;
-  load_tile(tile, p.x, p.rows, p.cols, p.ld, tr0, tc0);
-  __syncthreads();
-  if (y_col) {
-    const int cp = threadIdx.x & 127, h = threadIdx.x >> 7;
-    const int64_t col = tc0 + 2 * cp, row0 = tr0 + 32 * h;
-    if (col < p.cols && row0 < p.rows) {
-      float2 Pa[16], Pb[16];
+__global__ void __launch_bounds__(kNT, 2) rotate_bf16_kernel(const __grid_constant__ CUtensorMap tmx,
+                                                             const QuantParams p, uint16_t* y_row,
+                                                             uint16_t* y_col) {
+  tile_loop(&tmx, p.rows, p.cols, p.status, [&](const TileView& tv, int64_t tr0, int64_t tc0) {
+    if (y_col) {
+      const int cp = threadIdx.x & 127, h = threadIdx.x >> 7;
+      const int64_t col = tc0 + 2 * cp, row0 = tr0 + 32 * h;
+      if (col < p.cols && row0 < p.rows) {
+        float2 Pa[16], Pb[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t wa = tile_word(tile, 32 * h + i, cp), wb = tile_word(tile, 32 * h + i + 16, cp);
-        Pa[i].x = __uint_as_float((wa << 16) ^ p.sgn_col[i]);
-        Pa[i].y = __uint_as_float((wb << 16) ^ p.sgn_col[i + 16]);
-        Pb[i].x = __uint_as_float((wa & 0xFFFF0000u) ^ p.sgn_col[i]);
-        Pb[i].y = __uint_as_float((wb & 0xFFFF0000u) ^ p.sgn_col[i + 16]);
-      }
-      rotate_chunk<NH>(Pa);
-      rotate_chunk<NH>(Pb);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        uint32_t* o0 = reinterpret_cast<uint32_t*>(y_col + (row0 + i) * p.cols + col);
-        uint32_t* o1 = reinterpret_cast<uint32_t*>(y_col + (row0 + i + 16) * p.cols + col);
-        *o0 = f32_to_bf16_rne(Pa[i].x) | (f32_to_bf16_rne(Pb[i].x) << 16);
-        *o1 = f32_to_bf16_rne(Pa[i].y) | (f32_to_bf16_rne(Pb[i].y) << 16);
-      }
-    }
-  }
-  if (y_row) {
-#pragma unroll 1
-    for (int k = 0; k < (kTR * (kTC / 32)) / kNT; ++k) {
-      const int id = threadIdx.x + kNT * k;
-      const int r = id >> 3, q = id & 7;
-      const int64_t gr = tr0 + r, gc = tc0 + 32 * q;
-      if (gr < p.rows && gc < p.cols) {
-        float2 P[16];
-        read_row_chunk(tile, r, q, p.sgn_row, P);
-        rotate_chunk<NH>(P);
-        uint32_t o[16];
-#pragma unroll
-        for (int k2 = 0; k2 < 8; ++k2) {
-          o[k2] = f32_to_bf16_rne(P[2 * k2].x) | (f32_to_bf16_rne(P[2 * k2 + 1].x) << 16);
-          o[k2 + 8] = f32_to_bf16_rne(P[2 * k2].y) | (f32_to_bf16_rne(P[2 * k2 + 1].y) << 16);
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t wa = tv.word(32 * h + i, cp), wb = tv.word(32 * h + i + 16, cp);
+          Pa[i].x = __uint_as_float((wa << 16) ^ p.sgn_col[i]);
+          Pa[i].y = __uint_as_float((wb << 16) ^ p.sgn_col[i + 16]);
+          Pb[i].x = __uint_as_float((wa & 0xFFFF0000u) ^ p.sgn_col[i]);
+          Pb[i].y = __uint_as_float((wb & 0xFFFF0000u) ^ p.sgn_col[i + 16]);
         }
-        uint4* dst = reinterpret_cast<uint4*>(y_row + gr * p.cols + gc);
+        rotate_chunk<NH>(Pa);
+        rotate_chunk<NH>(Pb);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        for (int i = 0; i < 16; ++i) {
+          uint32_t* o0 = reinterpret_cast<uint32_t*>(y_col + (row0 + i) * p.cols + col);
+          uint32_t* o1 = reinterpret_cast<uint32_t*>(y_col + (row0 + i + 16) * p.cols + col);
+          *o0 = f32_to_bf16_rne(Pa[i].x) | (f32_to_bf16_rne(Pb[i].x) << 16);
+          *o1 = f32_to_bf16_rne(Pa[i].y) | (f32_to_bf16_rne(Pb[i].y) << 16);
+        }
       }
     }
-  }
+    if (y_row) {
+#pragma unroll 1
+      for (int k = 0; k < (kTR * (kTC / 32)) / kNT; ++k) {
+        int r, q;
+        row_task(threadIdx.x + kNT * k, r, q);
+        const int64_t gr = tr0 + r, gc = tc0 + 32 * q;
+        if (gr < p.rows && gc < p.cols) {
+          float2 P[16];
+          read_row_chunk(tv, r, q, p.sgn_row, P);
+          rotate_chunk<NH>(P);
+          uint32_t o[16];
+#pragma unroll
+          for (int k2 = 0; k2 < 8; ++k2) {
+            o[k2] = f32_to_bf16_rne(P[2 * k2].x) | (f32_to_bf16_rne(P[2 * k2 + 1].x) << 16);
+            o[k2 + 8] = f32_to_bf16_rne(P[2 * k2].y) | (f32_to_bf16_rne(P[2 * k2 + 1].y) << 16);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(y_row + gr * p.cols + gc);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        }
+      }
+    }
+  });
 }
 
 // ------------------------------------------------------------ launchers
-template <int GRID, int SCALE, int NH>
-static cudaError_t launch_quant_round(const QuantParams& p, int round, dim3 grid, cudaStream_t s) {
-  if (round == FP4Q_SR)
-    rht_quant_kernel<GRID, SCALE, NH, FP4Q_SR><<<grid, kNT, 0, s>>>(p);
-  else
-    rht_quant_kernel<GRID, SCALE, NH, FP4Q_RTNE><<<grid, kNT, 0, s>>>(p);
+// The input's tensor map: bf16 [rows][cols] with row stride ld, 64 x 64 boxes,
+// 128-byte swizzle, zero fill outside the matrix.
+static bool input_map(const QuantParams& p, CUtensorMap* m) {
+  return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.x, (uint64_t)p.cols, (uint64_t)p.rows,
+                        (uint64_t)p.ld * 2u, 64u, 64u, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+static unsigned persistent_grid(const QuantParams& p) {
+  const int64_t ntiles = ((p.cols + kTC - 1) / kTC) * ((p.rows + kTR - 1) / kTR);
+  const int64_t g = 2 * (int64_t)num_sms();
+  return (unsigned)(ntiles < g ? ntiles : g);
+}
+
+// Opt a kernel into the dynamic shared memory of the tile ring once.
+template <class K>
+static cudaError_t smem_attr(K kernel, bool& done) {
+  if (done) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQuantSmem);
+  if (e == cudaSuccess) done = true;
+  return e;
+}
+
+template <int GRID, int SCALE, int NH, int ROUND>
+static cudaError_t launch_quant_inst(const CUtensorMap& m, const QuantParams& p, cudaStream_t s) {
+  static bool attr = false;
+  cudaError_t e = smem_attr(rht_quant_kernel<GRID, SCALE, NH, ROUND>, attr);
+  if (e != cudaSuccess) return e;
+  rht_quant_kernel<GRID, SCALE, NH, ROUND><<<persistent_grid(p), kNT, kQuantSmem, s>>>(m, p);
   return cudaGetLastError();
 }
 
-template <int GRID, int SCALE>
-static cudaError_t launch_quant_nh(const QuantParams& p, int nh, int round, dim3 grid, cudaStream_t s) {
-  switch (nh) {
-    case 16: return launch_quant_round<GRID, SCALE, 16>(p, round, grid, s);
-    case 32: return launch_quant_round<GRID, SCALE, 32>(p, round, grid, s);
-    default: return launch_quant_round<GRID, SCALE, 0>(p, round, grid, s);
-  }
+template <int GRID, int SCALE, int NH>
+static cudaError_t launch_quant_round(const CUtensorMap& m, const QuantParams& p, int round, cudaStream_t s) {
+  return round == FP4Q_SR ? launch_quant_inst<GRID, SCALE, NH, FP4Q_SR>(m, p, s)
+                          : launch_quant_inst<GRID, SCALE, NH, FP4Q_RTNE>(m, p, s);
 }
 
-static dim3 tile_grid(int64_t rows, int64_t cols) {
-  return dim3((unsigned)((cols + kTC - 1) / kTC), (unsigned)((rows + kTR - 1) / kTR), 1);
+template <int GRID, int SCALE>
+static cudaError_t launch_quant_nh(const CUtensorMap& m, const QuantParams& p, int nh, int round, cudaStream_t s) {
+  switch (nh) {
+    case 16: return launch_quant_round<GRID, SCALE, 16>(m, p, round, s);
+    case 32: return launch_quant_round<GRID, SCALE, 32>(m, p, round, s);
+    default: return launch_quant_round<GRID, SCALE, 0>(m, p, round, s);
+  }
 }
 
 cudaError_t launch_rht_quant(const QuantParams& p, int grid_kind, int scale, int nh, int round,
                              cudaStream_t s) {
-  const dim3 g = tile_grid(p.rows, p.cols);
+  CUtensorMap m;
+  if (!input_map(p, &m)) return cudaErrorInvalidValue;
   if (grid_kind == FP4Q_GRID_E2M1) {
-    return scale == FP4Q_SCALE_NV ? launch_quant_nh<FP4Q_GRID_E2M1, FP4Q_SCALE_NV>(p, nh, round, g, s)
-                                  : launch_quant_nh<FP4Q_GRID_E2M1, FP4Q_SCALE_MX>(p, nh, round, g, s);
+    return scale == FP4Q_SCALE_NV ? launch_quant_nh<FP4Q_GRID_E2M1, FP4Q_SCALE_NV>(m, p, nh, round, s)
+                                  : launch_quant_nh<FP4Q_GRID_E2M1, FP4Q_SCALE_MX>(m, p, nh, round, s);
   }
-  return scale == FP4Q_SCALE_NV ? launch_quant_nh<FP4Q_GRID_E1M2, FP4Q_SCALE_NV>(p, nh, round, g, s)
-                                : launch_quant_nh<FP4Q_GRID_E1M2, FP4Q_SCALE_MX>(p, nh, round, g, s);
+  return scale == FP4Q_SCALE_NV ? launch_quant_nh<FP4Q_GRID_E1M2, FP4Q_SCALE_NV>(m, p, nh, round, s)
+                                : launch_quant_nh<FP4Q_GRID_E1M2, FP4Q_SCALE_MX>(m, p, nh, round, s);
+}
+
+template <int NH>
+static cudaError_t launch_amax_inst(const CUtensorMap& m, const QuantParams& p, float* amax, cudaStream_t s) {
+  static bool attr = false;
+  cudaError_t e = smem_attr(rotated_amax_kernel<NH>, attr);
+  if (e != cudaSuccess) return e;
+  rotated_amax_kernel<NH><<<persistent_grid(p), kNT, kQuantSmem, s>>>(m, p, amax);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_rotated_amax(const QuantParams& p, int nh, float* amax, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(amax, 0, 2 * sizeof(float), s);
   if (e != cudaSuccess) return e;
-  const dim3 g = tile_grid(p.rows, p.cols);
+  CUtensorMap m;
+  if (!input_map(p, &m)) return cudaErrorInvalidValue;
   switch (nh) {
-    case 16: rotated_amax_kernel<16><<<g, kNT, 0, s>>>(p, amax); break;
-    case 32: rotated_amax_kernel<32><<<g, kNT, 0, s>>>(p, amax); break;
-    default: rotated_amax_kernel<0><<<g, kNT, 0, s>>>(p, amax); break;
+    case 16: return launch_amax_inst<16>(m, p, amax, s);
+    case 32: return launch_amax_inst<32>(m, p, amax, s);
+    default: return launch_amax_inst<0>(m, p, amax, s);
   }
-  return cudaGetLastError();
 }
 
 template <int GRID, int SCALE>
@@ -628,14 +754,24 @@ cudaError_t launch_dequant(const DequantParams& d, int grid_kind, int scale, int
   return cudaGetLastError();
 }
 
-cudaError_t launch_rotate_bf16(const QuantParams& p, int nh, uint16_t* y_row, uint16_t* y_col, cudaStream_t s) {
-  const dim3 g = tile_grid(p.rows, p.cols);
-  switch (nh) {
-    case 16: rotate_bf16_kernel<16><<<g, kNT, 0, s>>>(p, y_row, y_col); break;
-    case 32: rotate_bf16_kernel<32><<<g, kNT, 0, s>>>(p, y_row, y_col); break;
-    default: rotate_bf16_kernel<0><<<g, kNT, 0, s>>>(p, y_row, y_col); break;
-  }
+template <int NH>
+static cudaError_t launch_rot_inst(const CUtensorMap& m, const QuantParams& p, uint16_t* yr, uint16_t* yc,
+                                   cudaStream_t s) {
+  static bool attr = false;
+  cudaError_t e = smem_attr(rotate_bf16_kernel<NH>, attr);
+  if (e != cudaSuccess) return e;
+  rotate_bf16_kernel<NH><<<persistent_grid(p), kNT, kQuantSmem, s>>>(m, p, yr, yc);
   return cudaGetLastError();
+}
+
+cudaError_t launch_rotate_bf16(const QuantParams& p, int nh, uint16_t* y_row, uint16_t* y_col, cudaStream_t s) {
+  CUtensorMap m;
+  if (!input_map(p, &m)) return cudaErrorInvalidValue;
+  switch (nh) {
+    case 16: return launch_rot_inst<16>(m, p, y_row, y_col, s);
+    case 32: return launch_rot_inst<32>(m, p, y_row, y_col, s);
+    default: return launch_rot_inst<0>(m, p, y_row, y_col, s);
+  }
 }
 
 }  // namespace fp4q
