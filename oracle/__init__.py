@@ -23,7 +23,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-GRID_E2M1, GRID_E1M2 = 0, 1
+GRID_E2M1, GRID_E1M2, GRID_E2M1_R4 = 0, 1, 2
 SCALE_MX, SCALE_NV = 0, 1
 RTNE, SR = 0, 1
 
@@ -56,6 +56,8 @@ def lib() -> ctypes.CDLL:
         L.orc_grid_qmax.argtypes = [i32]
         L.orc_grid_emax.restype = i32
         L.orc_grid_emax.argtypes = [i32]
+        L.orc_grid_top.restype = i32
+        L.orc_grid_top.argtypes = [i32]
         L.orc_code_value.restype = ctypes.c_float
         L.orc_code_value.argtypes = [i32, i32]
         L.orc_bf16_to_f32.restype = ctypes.c_float
@@ -105,6 +107,10 @@ def grid_qmax(grid: int) -> float:
 
 def grid_emax(grid: int) -> int:
     return int(lib().orc_grid_emax(grid))
+
+
+def grid_top(grid: int) -> int:
+    return int(lib().orc_grid_top(grid))
 
 
 def code_value(grid: int, code: int) -> float:

@@ -34,7 +34,7 @@
 /* ------------------------------------------------------------------------ */
 /* Enumerations, mirrored by value in oracle/__init__.py                     */
 /* ------------------------------------------------------------------------ */
-enum { ORC_GRID_E2M1 = 0, ORC_GRID_E1M2 = 1 };
+enum { ORC_GRID_E2M1 = 0, ORC_GRID_E1M2 = 1, ORC_GRID_E2M1_R4 = 2 };
 enum { ORC_SCALE_MX = 0, ORC_SCALE_NV = 1 };
 enum { ORC_RTNE = 0, ORC_SR = 1 };
 
@@ -52,18 +52,32 @@ static const float E2M1_LEVELS[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6
  * left and right bin width agree ([SB] Metodologia 2, "Grade Uniforme"). */
 static const float E1M2_LEVELS[8] = {0.0f, 0.25f, 0.5f, 0.75f, 1.0f, 1.25f, 1.5f, 1.75f};
 
+/* Range-restricted E2M1 ([SB] Resultados, ablation "Restricao de Alcance":
+ * E2M1 with its largest values cut to mimic a uniform grid).  Reading: the
+ * maximum is capped at 4 (levels 0 .. 4, codes 0..6 -- still E2M1 bit
+ * patterns, decoded with the E2M1 table), and the shared exponent uses
+ * e_max = 1 so that block maxima land in [2, 4) and never clip. */
+
 float orc_grid_level(int grid, int k)
 {
     if (k < 0 || k > 7) return NAN;
     return grid == ORC_GRID_E1M2 ? E1M2_LEVELS[k] : E2M1_LEVELS[k];
 }
 
-/* Largest magnitude of the grid. */
-float orc_grid_qmax(int grid) { return orc_grid_level(grid, 7); }
+/* Index of the largest code a grid produces (7, or 6 for the capped grid). */
+int orc_grid_top(int grid) { return grid == ORC_GRID_E2M1_R4 ? 6 : 7; }
 
-/* Exponent of the largest power of two not above q_max: 2 for E2M1 (4 <= 6),
- * 0 for E1M2 (1 <= 1.75). */
-int orc_grid_emax(int grid) { return grid == ORC_GRID_E1M2 ? 0 : 2; }
+/* Largest magnitude of the grid. */
+float orc_grid_qmax(int grid) { return orc_grid_level(grid, orc_grid_top(grid)); }
+
+/* Exponent of the power of two the block maximum is scaled to: 2 for E2M1
+ * (largest power of two not above 6), 0 for E1M2 (1 <= 1.75), 1 for the
+ * capped grid (block maxima in [2, 4)). */
+int orc_grid_emax(int grid)
+{
+    if (grid == ORC_GRID_E1M2) return 0;
+    return grid == ORC_GRID_E2M1_R4 ? 1 : 2;
+}
 
 /* Value of a 4-bit code: bit 3 is the sign, bits 0..2 the magnitude index. */
 float orc_code_value(int grid, int code)
@@ -245,15 +259,16 @@ int orc_round_rtne(int grid, float v)
 {
     int sign = signbit(v) ? 8 : 0;
     float a = fabsf(v);
+    int top = orc_grid_top(grid);
     float qmax = orc_grid_qmax(grid);
-    if (!(a < qmax)) return sign | 7;
-    for (int k = 0; k < 7; ++k) {
+    if (!(a < qmax)) return sign | top;
+    for (int k = 0; k < top; ++k) {
         float lo = orc_grid_level(grid, k), hi = orc_grid_level(grid, k + 1);
-        float mid = (lo + hi) * 0.5f; /* exact for both grids */
+        float mid = (lo + hi) * 0.5f; /* exact for every grid */
         if (a < mid) return sign | k;
         if (a == mid) return sign | ((k & 1) ? k + 1 : k);
     }
-    return sign | 7;
+    return sign | top;
 }
 
 /* Stochastic rounding ([SB] Metodologia 2: SR on dY only, to preserve the
@@ -265,9 +280,10 @@ int orc_round_sr(int grid, float v, uint32_t r16)
 {
     int sign = signbit(v) ? 8 : 0;
     float a = fabsf(v);
+    int top = orc_grid_top(grid);
     float qmax = orc_grid_qmax(grid);
-    if (!(a < qmax)) return sign | 7;
-    for (int k = 0; k < 7; ++k) {
+    if (!(a < qmax)) return sign | top;
+    for (int k = 0; k < top; ++k) {
         float lo = orc_grid_level(grid, k), hi = orc_grid_level(grid, k + 1);
         if (a >= lo && a < hi) {
             float f = (a - lo) / (hi - lo); /* exact: Sterbenz and a power-of-two gap */
@@ -275,7 +291,7 @@ int orc_round_sr(int grid, float v, uint32_t r16)
             return sign | (u < f ? k + 1 : k);
         }
     }
-    return sign | 7;
+    return sign | top;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -289,7 +305,7 @@ int orc_round_sr(int grid, float v, uint32_t r16)
  *               transposed (C x R/2 code bytes, C x R/b scale bytes).  It is
  *               formed by transposing the input and quantizing its rows.
  *
- *   grid      ORC_GRID_E2M1 or ORC_GRID_E1M2
+ *   grid      ORC_GRID_E2M1, ORC_GRID_E1M2 or ORC_GRID_E2M1_R4
  *   scale     ORC_SCALE_MX: b = 32, E8M0 shared exponent ([HTX] Que es MXFP4?)
  *             ORC_SCALE_NV: b = 16, E4M3 block scale, fp32 tensor scale,
  *             v = y * fl(1 / (sb * S_t)) per element

@@ -125,3 +125,13 @@ def test_sr_uniform_stream_chi2(orc):
     assert r[0] == (w[0] & 0xFFFF) and r[1] == (w[0] >> 16) and r[7] == (w[3] >> 16)
     # orientation changes the stream
     assert [orc.sr_uniform16(99, i, 1) for i in range(8)] != list(r[:8])
+
+
+def test_capped_e2m1_is_e2m1_without_its_top_level(orc):
+    """The range-restricted grid decodes with the E2M1 table, never produces
+    code 7 (6.0), saturates at 4 and scales block maxima into [2, 4)."""
+    e2 = [_decode_minifloat(k, 2, 1, 1) for k in range(8)]
+    assert list(orc.grid_levels(orc.GRID_E2M1_R4)) == e2
+    assert orc.grid_top(orc.GRID_E2M1_R4) == 6 and orc.grid_qmax(orc.GRID_E2M1_R4) == 4.0
+    assert orc.grid_emax(orc.GRID_E2M1_R4) == 1
+    assert max(orc.round_rtne(2, float(v)) & 7 for v in np.linspace(0, 100, 1001)) == 6

@@ -7,8 +7,9 @@ import pytest
 from fp4_microscaled_quantization_gb300 import synth
 
 LEVELS = {0: np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6], np.float64),
-          1: np.array([0, 0.25, 0.5, 0.75, 1, 1.25, 1.5, 1.75], np.float64)}
-EMAX = {0: 2, 1: 0}
+          1: np.array([0, 0.25, 0.5, 0.75, 1, 1.25, 1.5, 1.75], np.float64),
+          2: np.array([0, 0.5, 1, 1.5, 2, 3, 4], np.float64)}      # E2M1 capped at 4
+EMAX = {0: 2, 1: 0, 2: 1}
 
 
 def unpack(codes: np.ndarray) -> np.ndarray:
@@ -26,7 +27,7 @@ def rotated_rows(orc, x_bits, n_h, mask):
     return y
 
 
-@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("grid", [0, 1, 2])
 @pytest.mark.parametrize("n_h", [0, 16, 32])
 def test_mx_exponent_closed_form_and_nearest_code(orc, grid, n_h):
     x = synth.special_values(64, 128, 11)
@@ -54,7 +55,7 @@ def test_mx_exponent_closed_form_and_nearest_code(orc, grid, n_h):
                 c = int(codes[r, kb * 32 + t])
                 a = abs(v)
                 if a >= L[-1]:
-                    assert c & 7 == 7
+                    assert c & 7 == len(L) - 1
                 else:
                     d = np.abs(a - L)
                     cand = np.flatnonzero(d == d.min())
@@ -77,7 +78,7 @@ def test_all_zero_block_and_packing(orc):
     assert q["scales"][0, 1] == 127 + 0      # m = 6: floor(log2 6) - 2 = 0
 
 
-@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("grid", [0, 1, 2])
 def test_mx_dequant_is_exact(orc, grid):
     x = synth.special_values(32, 256, 12)
     q = orc.quantize(x, 0, grid, orc.SCALE_MX, 16, 0)
@@ -88,7 +89,7 @@ def test_mx_dequant_is_exact(orc, grid):
     assert np.array_equal(d.astype(np.float64), want)
 
 
-@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("grid", [0, 1, 2])
 @pytest.mark.parametrize("n_h", [16, 32])
 def test_nv_invariants(orc, grid, n_h):
     x = synth.normal(64, 256, 21, 0.02)
@@ -128,7 +129,7 @@ def test_nv_zero_tensor_and_given_amax(orc):
     assert q2["scales"].max() < 0x7E
 
 
-@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("grid", [0, 1, 2])
 def test_e4m3_bytes_hold_the_code_values(orc, grid):
     x = synth.special_values(32, 128, 5)
     q = orc.quantize(x, 0, grid, orc.SCALE_MX, 16, 0, want_e4m3=True)
