@@ -18,7 +18,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 bool valid_cfg(const fp4q_config* c) {
   if (!c) return false;
-  if (c->grid != FP4Q_GRID_E2M1 && c->grid != FP4Q_GRID_E1M2) return false;
+  if (c->grid != FP4Q_GRID_E2M1 && c->grid != FP4Q_GRID_E1M2 && c->grid != FP4Q_GRID_E2M1_R4) return false;
   if (c->scale != FP4Q_SCALE_MX && c->scale != FP4Q_SCALE_NV) return false;
   if (c->rot != FP4Q_ROT_NONE && c->rot != FP4Q_ROT_H16 && c->rot != FP4Q_ROT_H32) return false;
   if (c->round != FP4Q_RTNE && c->round != FP4Q_SR) return false;

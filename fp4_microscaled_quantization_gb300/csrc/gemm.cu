@@ -32,6 +32,10 @@
 #include "fp4q_dev.cuh"
 #include "fp4q_internal.h"
 
+#ifndef FP4Q_GEMM_PAIR
+#define FP4Q_GEMM_PAIR 0
+#endif
+
 namespace fp4q {
 namespace {
 
@@ -185,12 +189,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 // Instruction descriptor of the block-scaled kinds: B scale id in bits 4-5,
 // A/B element types in 7-9 / 10-12, K-major A and B, N >> 3 in 17-22, scale
 // type in 23 (1 = E8M0, 0 = E4M3), M >> 4 in 24-28, A scale id in 29-30.
-template <int KIND>
+template <int KIND, int MM = BM>
 __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
   constexpr uint32_t ty = KIND == KIND_F8 ? 0u : 1u;   // E4M3 (f8f6f4) or E2M1 (mxf4 kinds)
   constexpr uint32_t sfmt = KIND == KIND_NVF4 ? 0u : 1u;
   return (sf_id << 4) | (ty << 7) | (ty << 10) | ((uint32_t)(BN >> 3) << 17) | (sfmt << 23) |
-         ((uint32_t)(BM >> 4) << 24) | (sf_id << 29);
+         ((uint32_t)(MM >> 4) << 24) | (sf_id << 29);
 }
 
 // ------------------------------------------------------------ the kernel
@@ -422,11 +426,375 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
+
+// ------------------------------------------------------------ CTA-pair kernel
+// Two CTAs of a cluster share one 256 x 256 output tile through
+// tcgen05.mma.cta_group::2 (M = 256 across the pair, N = 256): each CTA loads
+// its own 128 rows of A and its own 128-row half of B (so each SM moves 32 KB
+// of operands per K-tile instead of 48 KB), plus the scale chunks of its A rows
+// and of both B row groups, and signals the leader CTA's full barrier
+// (cp.async.bulk.tensor ... .cta_group::2).  The leader (cluster rank 0)
+// copies scales to TMEM and issues the MMAs for both; commits are multicast to
+// both CTAs' empty / accumulator barriers; each CTA's epilogue drains its own
+// 128 accumulator rows and releases them with an arrive on the leader.
+namespace pairk {
+
+constexpr int A_BYTES = 128 * KROW;   // this CTA's 128 rows of A
+constexpr int B_BYTES = 128 * KROW;   // this CTA's half of B
+
+template <int KIND>
+struct Layout {
+  static constexpr int kSfChunk = KindK<KIND>::kChunksPerTile * 512;   // one row group, one K-tile
+  static constexpr int SFA_OFF = A_BYTES + B_BYTES;
+  static constexpr int SFB_OFF = SFA_OFF + kSfChunk;
+  static constexpr int STAGE = ((SFB_OFF + 2 * kSfChunk) + 1023) / 1024 * 1024;
+  static constexpr int STAGES = KIND == KIND_NVF4 ? 5 : 6;
+  static constexpr int BAR_OFF = STAGES * STAGE;
+  static constexpr int SMEM = BAR_OFF + 256 + 1024;
+  static constexpr uint32_t SF_COLS = 12u * KindK<KIND>::kChunksPerTile;   // SFA 4/chunk + SFB 8/chunk
+  static constexpr uint32_t TX = A_BYTES + B_BYTES + 3 * kSfChunk;        // bytes one CTA lands per stage
+  static_assert(BAR_OFF + 256 + 1024 <= 232448, "shared memory");
+  static_assert(256 + STAGES * SF_COLS <= TMEM_COLS, "tensor memory");
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void remote_expect_tx(uint32_t cluster_bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* tm, int32_t x, int32_t y,
+                                                 uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(dst),
+      "l"(tm), "r"(x), "r"(y), "r"(cluster_bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_cp_sf2(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+__device__ __forceinline__ void tc_commit2(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+template <int KIND>
+__device__ __forceinline__ void tc_mma2(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                        uint32_t sfb, uint32_t acc) {
+  if constexpr (KIND == KIND_MXF4) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p; }"
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+        : "memory");
+  } else if constexpr (KIND == KIND_NVF4) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p; }"
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+        : "memory");
+  } else {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p; }"
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+        : "memory");
+  }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                        const GemmParams p) {
+  using KK = KindK<KIND>;
+  using L = Layout<KIND>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar_full = sbase + L::BAR_OFF;
+  const uint32_t bar_empty = bar_full + 8 * L::STAGES;
+  const uint32_t bar_acc_full = bar_empty + 8 * L::STAGES;
+  const uint32_t bar_acc_empty = bar_acc_full + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + 16 * L::STAGES + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR_OFF + 16 * L::STAGES + 24);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int n_blocks = (p.N + 255) / 256;
+  const int n_tiles = ((p.M + 255) / 256) * n_blocks;
+  const int num_kt = (p.K + KK::kElemsPerTile - 1) / KK::kElemsPerTile;
+  const int nq = p.K / KK::kBlock / 4;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < L::STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 2);    // one expect_tx arrival from each CTA's producer
+      mbar_init(bar_empty + 8 * s, 1);   // the leader's multicast commit
+    }
+    mbar_init(bar_acc_full, 1);
+    mbar_init(bar_acc_empty, 8);         // every epilogue warp of both CTAs
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t lead_full = mapa(bar_full, 0);
+  const uint32_t lead_acc_empty = mapa(bar_acc_empty, 0);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- producer (both CTAs)
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
+      uint32_t it = 0;
+      for (int tile = pair; tile < n_tiles && !*abort_flag; tile += npairs) {
+        const int m0 = (tile / n_blocks) * 256, n0 = (tile % n_blocks) * 256;
+        for (int kt = 0; kt < num_kt; ++kt, ++it) {
+          const int s = (int)(it % L::STAGES);
+          const uint32_t ph = (it / L::STAGES) & 1u;
+          if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag)) {
+            *abort_flag = 1;
+            raise_status(p.status, FP4Q_DEV_TIMEOUT);
+            break;
+          }
+          const uint32_t st = sbase + (uint32_t)s * L::STAGE;
+          const uint32_t fb = lead_full + 8 * s;
+          const int q0 = kt * KK::kChunksPerTile;
+          remote_expect_tx(fb, L::TX);
+          tma_load_2d_pair(st, &tmA, kt * KROW, m0 + 128 * (int)rank, fb);
+          tma_load_2d_pair(st + A_BYTES, &tmB, kt * KROW, n0 + 128 * (int)rank, fb);
+          tma_load_2d_pair(st + L::SFA_OFF, &tmSA, 0, (m0 / 128 + (int)rank) * nq + q0, fb);
+          tma_load_2d_pair(st + L::SFB_OFF, &tmSB, 0, (n0 / 128) * nq + q0, fb);
+          tma_load_2d_pair(st + L::SFB_OFF + L::kSfChunk, &tmSB, 0, (n0 / 128 + 1) * nq + q0, fb);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ---------------- MMA issuer (leader only)
+      uint32_t it = 0, tl = 0;
+      for (int tile = pair; tile < n_tiles; tile += npairs, ++tl) {
+        if (!mbar_wait(bar_acc_empty, (tl & 1u) ^ 1u, abort_flag)) {
+          *abort_flag = 1;
+          raise_status(p.status, FP4Q_DEV_TIMEOUT);
+          break;
+        }
+        tc_fence_after();
+        bool ok = true;
+        for (int kt = 0; kt < num_kt; ++kt, ++it) {
+          const int s = (int)(it % L::STAGES);
+          const uint32_t ph = (it / L::STAGES) & 1u;
+          if (!mbar_wait(bar_full + 8 * s, ph, abort_flag)) {
+            *abort_flag = 1;
+            raise_status(p.status, FP4Q_DEV_TIMEOUT);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = sbase + (uint32_t)s * L::STAGE;
+          const uint32_t sfa_col = tmem + 256 + L::SF_COLS * (uint32_t)s;
+          const uint32_t sfb_col = sfa_col + 4 * KK::kChunksPerTile;
+          const int q0 = kt * KK::kChunksPerTile;
+          const int nch = min(KK::kChunksPerTile, nq - q0);
+          for (int c = 0; c < nch; ++c) {
+            tc_cp_sf2(sfa_col + 4 * c, sf_desc(st + L::SFA_OFF + 512 * c));
+            tc_cp_sf2(sfb_col + 8 * c, sf_desc(st + L::SFB_OFF + 512 * c));
+            tc_cp_sf2(sfb_col + 8 * c + 4, sf_desc(st + L::SFB_OFF + L::kSfChunk + 512 * c));
+          }
+          const int rem = p.K - kt * KK::kElemsPerTile;
+          const int n_mma = min(4, rem / KK::kMmaK);
+          for (int k = 0; k < n_mma; ++k) {
+            uint32_t sfa = sfa_col, sfb = sfb_col, sf_id = 0;
+            if constexpr (KIND == KIND_MXF4) {
+              sfa += 4 * (k >> 1);
+              sfb += 8 * (k >> 1);
+              sf_id = 2u * (uint32_t)(k & 1);
+            } else if constexpr (KIND == KIND_NVF4) {
+              sfa += 4 * k;
+              sfb += 8 * k;
+            } else {
+              sf_id = (uint32_t)k;
+            }
+            tc_mma2<KIND>(tmem + ACC_COL, op_desc(st + 32 * k), op_desc(st + A_BYTES + 32 * k),
+                          make_idesc<KIND, 256>(sf_id), sfa, sfb, (kt > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit2(bar_empty + 8 * s);
+        }
+        if (!ok) break;
+        tc_commit2(bar_acc_full);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue (both CTAs; warps 2..5 -> TMEM lane quarters 2, 3, 0, 1)
+    const int sp = warp & 3;
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * sp) << 16) + ACC_COL;
+    float alpha = 1.0f;
+    if constexpr (KIND == KIND_NVF4) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
+    uint32_t tl = 0;
+    for (int tile = pair; tile < n_tiles; tile += npairs, ++tl) {
+      const int m0 = (tile / n_blocks) * 256 + 128 * (int)rank, n0 = (tile % n_blocks) * 256;
+      const int row = m0 + 32 * sp + lane;
+      bool ok = mbar_wait(bar_acc_full, tl & 1u, abort_flag);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          raise_status(p.status, FP4Q_DEV_TIMEOUT);
+        }
+        break;
+      }
+      tc_fence_after();
+      const int ncols = min(BN, p.N - n0);
+      const bool live = m0 < p.M;   // the follower's rows of a 128-row tail tile lie outside the matrix
+      if (p.d_f32 == nullptr) {
+        uint32_t h[BN / 2];
+#pragma unroll
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          if (c0 < ncols) {
+            uint32_t r[32];
+            tmem_ld32(lane_base + (uint32_t)c0, r);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              float a = __uint_as_float(r[2 * j]), b = __uint_as_float(r[2 * j + 1]);
+              if constexpr (KIND == KIND_NVF4) {
+                a = __fmul_rn(a, alpha);
+                b = __fmul_rn(b, alpha);
+              }
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(a, b);
+              h[c0 / 2 + j] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) remote_arrive(lead_acc_empty);
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(p.d_bf16 + (size_t)row * p.N + n0);
+#pragma unroll
+          for (int j = 0; j < BN / 8; ++j)
+            if (8 * j < ncols) dst[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+        }
+      } else {
+        for (int c0 = 0; c0 < ncols; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(lane_base + (uint32_t)c0, r);
+          if (!live) continue;
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            v[j] = __uint_as_float(r[j]);
+            if constexpr (KIND == KIND_NVF4) v[j] = __fmul_rn(v[j], alpha);
+          }
+          const size_t off = (size_t)row * p.N + n0 + c0;
+          float4* df = reinterpret_cast<float4*>(p.d_f32 + off);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) df[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          if (p.d_bf16) {
+            uint32_t hb[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+              hb[j] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            uint4* db = reinterpret_cast<uint4*>(p.d_bf16 + off);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) db[j] = make_uint4(hb[4 * j], hb[4 * j + 1], hb[4 * j + 2], hb[4 * j + 3]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) remote_arrive(lead_acc_empty);
+      }
+    }
+  }
+  // No CTA may leave while its peer can still read its shared memory or
+  // tensor memory: meet, then free the pair's allocation together.
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+}  // namespace pairk
+
 // ------------------------------------------------------------ host side
 // 2-D byte tensor [rows][row_bytes], box = 128 bytes x box_rows, 128B swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
   return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, (uint32_t)KROW,
                         box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Scale factors in the MMA layout viewed as a 2-D u32 tensor: one row per
+// 512-byte chunk (rows / 128 * blocks / 4 chunks), box = chunks of one K-tile.
+bool make_sf_map(CUtensorMap* m, const void* base, uint64_t n_chunks, uint32_t box_chunks) {
+  return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, base, 128u, n_chunks, 512u, 128u, box_chunks,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+template <int KIND>
+cudaError_t launch_gemm_pair(const fp4q_operand* A, const fp4q_operand* B, const void* a_data, const void* b_data,
+                             uint64_t row_bytes, const GemmParams& p, cudaStream_t s) {
+  using L = pairk::Layout<KIND>;
+  CUtensorMap ta, tb, tsa, tsb;
+  const uint64_t nq = (uint64_t)p.K / KindK<KIND>::kBlock / 4;
+  if (!make_map(&ta, a_data, row_bytes, (uint64_t)p.M, 128) || !make_map(&tb, b_data, row_bytes, (uint64_t)p.N, 128) ||
+      !make_sf_map(&tsa, A->scales, (uint64_t)p.M / 128 * nq, KindK<KIND>::kChunksPerTile) ||
+      !make_sf_map(&tsb, B->scales, (uint64_t)p.N / 128 * nq, KindK<KIND>::kChunksPerTile))
+    return cudaErrorInvalidValue;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(pairk::bs_gemm_pair_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int tiles = ((p.M + 255) / 256) * ((p.N + 255) / 256);
+  int pairs = num_sms() / 2;
+  if (tiles < pairs) pairs = tiles;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = L::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pairk::bs_gemm_pair_kernel<KIND>, ta, tb, tsa, tsb, p);
 }
 
 template <int KIND>
@@ -453,7 +821,7 @@ extern "C" int32_t fp4q_gemm(const fp4q_operand* A, const fp4q_operand* B, int64
                              void* stream) {
   using namespace fp4q;
   if (!A || !B || (!D_bf16 && !D_f32)) return FP4Q_ERR_INVALID_ARG;
-  if (grid != FP4Q_GRID_E2M1 && grid != FP4Q_GRID_E1M2) return FP4Q_ERR_INVALID_ARG;
+  if (grid != FP4Q_GRID_E2M1 && grid != FP4Q_GRID_E1M2 && grid != FP4Q_GRID_E2M1_R4) return FP4Q_ERR_INVALID_ARG;
   if (scale != FP4Q_SCALE_MX && scale != FP4Q_SCALE_NV) return FP4Q_ERR_INVALID_ARG;
   if (grid == FP4Q_GRID_E1M2 && scale == FP4Q_SCALE_NV) return FP4Q_ERR_UNSUPPORTED;
   if (M <= 0 || N <= 0 || K <= 0) return FP4Q_ERR_INVALID_ARG;
@@ -468,9 +836,6 @@ extern "C" int32_t fp4q_gemm(const fp4q_operand* A, const fp4q_operand* B, int64
   if (!al(a_data, 16) || !al(b_data, 16) || !al(A->scales, 16) || !al(B->scales, 16)) return FP4Q_ERR_ALIGNMENT;
   if ((D_bf16 && !al(D_bf16, 16)) || (D_f32 && !al(D_f32, 16))) return FP4Q_ERR_ALIGNMENT;
   const uint64_t row_bytes = kind == KIND_F8 ? (uint64_t)K : (uint64_t)K / 2;
-  CUtensorMap ta, tb;
-  if (!make_map(&ta, a_data, row_bytes, (uint64_t)M, BM) || !make_map(&tb, b_data, row_bytes, (uint64_t)N, BN))
-    return FP4Q_ERR_CUDA;
   GemmParams p;
   p.sfa = A->scales;
   p.sfb = B->scales;
@@ -484,8 +849,17 @@ extern "C" int32_t fp4q_gemm(const fp4q_operand* A, const fp4q_operand* B, int64
   p.K = (int32_t)K;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
+#if FP4Q_GEMM_PAIR
+  if (kind == KIND_MXF4) e = launch_gemm_pair<KIND_MXF4>(A, B, a_data, b_data, row_bytes, p, s);
+  else if (kind == KIND_NVF4) e = launch_gemm_pair<KIND_NVF4>(A, B, a_data, b_data, row_bytes, p, s);
+  else e = launch_gemm_pair<KIND_F8>(A, B, a_data, b_data, row_bytes, p, s);
+#else
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, a_data, row_bytes, (uint64_t)M, BM) || !make_map(&tb, b_data, row_bytes, (uint64_t)N, BN))
+    return FP4Q_ERR_CUDA;
   if (kind == KIND_MXF4) e = launch_gemm<KIND_MXF4>(ta, tb, p, s);
   else if (kind == KIND_NVF4) e = launch_gemm<KIND_NVF4>(ta, tb, p, s);
   else e = launch_gemm<KIND_F8>(ta, tb, p, s);
+#endif
   return e == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
 }

@@ -13,9 +13,9 @@
 //         E8M0 shared exponent, nearest 4-bit value).
 //
 // Design (GB300-first, HBM-bound):
-//   * Persistent CTAs (two per SM) walk 64 x 256 bf16 tiles (32 KB).  Each
-//     tile is read once from HBM by TMA into a 3-stage shared-memory ring
-//     (128-byte swizzle), so two tiles are in flight while one is computed.
+//   * Persistent CTAs (three per SM) walk 32 x 256 bf16 tiles (16 KB).  Each
+//     tile is read once from HBM by TMA into a 4-stage shared-memory ring
+//     (128-byte swizzle), so three tiles are in flight while one is computed.
 //     Both the row-wise copy (blocks along columns) and the column-wise copy
 //     (blocks along rows, stored transposed) come from that one read.
 //   * A "chunk" is 32 consecutive elements of one row or one column.  A thread
@@ -36,7 +36,13 @@
 
 namespace fp4q {
 
-constexpr int kTR = 64;    // tile rows
+#ifndef QUANT_STAGES
+#define QUANT_STAGES 4       // tiles in flight per CTA
+#endif
+#ifndef QUANT_MIN_CTAS
+#define QUANT_MIN_CTAS 3     // resident CTAs per SM the register budget is sized for
+#endif
+constexpr int kTR = 32;    // tile rows
 constexpr int kTC = 256;   // tile columns
 constexpr int kNT = 256;   // threads per CTA
 
@@ -54,6 +60,21 @@ struct GridK<FP4Q_GRID_E1M2> {
   static constexpr int kEmax = 0;
   static constexpr uint32_t kE4T0 = 0x34302800u, kE4T1 = 0x3E3C3A38u;
 };
+// E2M1 capped at 4: E2M1 codes 0..6, block maxima scaled into [2, 4).
+template <>
+struct GridK<FP4Q_GRID_E2M1_R4> {
+  static constexpr float kQmax = 4.0f;
+  static constexpr int kEmax = 1;
+  static constexpr uint32_t kE4T0 = 0x3C383000u, kE4T1 = 0x4C484440u;
+};
+
+// Eight packed E2M1 codes with magnitude 7 (6.0) turned into 6 (4.0): the
+// saturation of the capped grid applied after the hardware conversion.
+__device__ __forceinline__ uint32_t cap_e2m1_codes(uint32_t w) {
+  const uint32_t m = w & 0x77777777u;
+  const uint32_t seven = m & (m >> 1) & (m >> 2) & 0x11111111u;   // bit 0 of each nibble whose low 3 bits are 111
+  return w ^ seven;
+}
 
 // ------------------------------------------------------------ rounding
 // RTNE onto {k/4}: clamp |v| to 1.75, then k = RNE(4|v|) read from the low
@@ -89,8 +110,9 @@ __device__ __forceinline__ uint32_t sr_e1m2(float v, float rf) {
 // SR onto E2M1: with E = clamp(floor(log2 |v|), 0, 2) the levels around |v|
 // are 2^(E-1) apart, s = |v| 2^(1-E) is exact, and the lower level's code is
 // 2E + floor(s) (floor(s) = 0..3 for E = 0, 2..3 above).
+template <int CAP = 6>
 __device__ __forceinline__ uint32_t sr_e2m1(float v, float rf) {
-  const float a = fminf(fabsf(v), 6.0f);
+  const float a = fminf(fabsf(v), (float)CAP);
   const uint32_t eb = __float_as_uint(fmaxf(a, 1.0f)) & 0x7F800000u;   // (127 + E) << 23
   const float s = a * __uint_as_float(0x7F800000u - eb);              // 2^(1-E), exponent 128 - E
   const uint32_t twoE = (eb >> 22) - 254u;
@@ -195,11 +217,15 @@ __device__ __forceinline__ void quantize_chunk(float2 (&P)[16], float S_t, uint6
 #pragma unroll
   for (int i = 0; i < 16; ++i) P[i] = mul2(P[i], vm);
 
-  if constexpr (ROUND == FP4Q_RTNE && GRID == FP4Q_GRID_E2M1) {
+  if constexpr (ROUND == FP4Q_RTNE && GRID != FP4Q_GRID_E1M2) {
     o.w[0] = cvt_e2m1x8(P[0].x, P[1].x, P[2].x, P[3].x, P[4].x, P[5].x, P[6].x, P[7].x);
     o.w[1] = cvt_e2m1x8(P[8].x, P[9].x, P[10].x, P[11].x, P[12].x, P[13].x, P[14].x, P[15].x);
     o.w[2] = cvt_e2m1x8(P[0].y, P[1].y, P[2].y, P[3].y, P[4].y, P[5].y, P[6].y, P[7].y);
     o.w[3] = cvt_e2m1x8(P[8].y, P[9].y, P[10].y, P[11].y, P[12].y, P[13].y, P[14].y, P[15].y);
+    if constexpr (GRID == FP4Q_GRID_E2M1_R4) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) o.w[q] = cap_e2m1_codes(o.w[q]);
+    }
   } else if constexpr (ROUND == FP4Q_RTNE) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -226,7 +252,8 @@ __device__ __forceinline__ void quantize_chunk(float2 (&P)[16], float S_t, uint6
         const int t = q * 8 + j;
         const float v = (t < 16) ? P[t].x : P[t - 16].y;
         const float rf = r16_float((j & 1) ? (r.v[j >> 1] >> 16) : (r.v[j >> 1] & 0xFFFFu));
-        const uint32_t code = (GRID == FP4Q_GRID_E1M2) ? sr_e1m2(v, rf) : sr_e2m1(v, rf);
+        const uint32_t code = (GRID == FP4Q_GRID_E1M2) ? sr_e1m2(v, rf)
+                              : (GRID == FP4Q_GRID_E2M1_R4) ? sr_e2m1<4>(v, rf) : sr_e2m1<6>(v, rf);
         w |= code << (4 * j);
       }
       o.w[q] = w;
@@ -266,25 +293,26 @@ __device__ __forceinline__ void store_chunk(const CopyOut& d, int64_t r, int64_t
 }
 
 // ------------------------------------------------------------ tile pipeline
-// Tiles of kTR x kTC bf16 arrive by TMA as four 64-row x 64-column boxes with
-// the 128-byte swizzle: within box b, logical row r occupies bytes
+// Tiles of kTR x kTC bf16 arrive by TMA as four kTR-row x 64-column boxes
+// with the 128-byte swizzle: within box b, logical row r occupies bytes
 // [r*128, r*128+128) and its 16-byte unit c sits at unit c ^ (r & 7).  The
-// thread <-> data mappings below keep both access patterns conflict-free:
-// eight threads of a quarter-warp read eight different rows of one row-wise
-// chunk (distinct r & 7), and a warp reads 32 consecutive words of one row.
-constexpr int kStages = 3;                       // tiles in flight per CTA
-constexpr int kTileBytes = kTR * kTC * 2;        // 32 KB
+// thread <-> data mappings keep both access patterns conflict-free: eight
+// threads of a quarter-warp read eight different rows of one row-wise chunk
+// (distinct r & 7), and a warp reads 32 consecutive columns of one row.
+constexpr int kStages = QUANT_STAGES;              // tiles in flight per CTA
+constexpr int kBoxBytes = kTR * 128;               // one 64-column box
+constexpr int kTileBytes = kTR * kTC * 2;          // 16 KB
 constexpr int kQuantSmem = kStages * kTileBytes + 1024 + 64;
 
 struct TileView {
   const uint8_t* t;
   // 16-byte unit u (0..31) of logical tile row r
   __device__ __forceinline__ uint4 unit(int r, int u) const {
-    return *reinterpret_cast<const uint4*>(t + ((u >> 3) << 13) + (r << 7) + (((u & 7) ^ (r & 7)) << 4));
+    return *reinterpret_cast<const uint4*>(t + (u >> 3) * kBoxBytes + (r << 7) + (((u & 7) ^ (r & 7)) << 4));
   }
   // word holding columns 2p, 2p+1 of tile row r (p = 0..127)
   __device__ __forceinline__ uint32_t word(int r, int p) const {
-    return *reinterpret_cast<const uint32_t*>(t + ((p >> 5) << 13) + (r << 7) +
+    return *reinterpret_cast<const uint32_t*>(t + (p >> 5) * kBoxBytes + (r << 7) +
                                               ((((p >> 2) & 7) ^ (r & 7)) << 4) + ((p & 3) << 2));
   }
 };
@@ -312,6 +340,82 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
   }
 }
 
+// Persistent walk over the tiles of the matrix: CTA b takes tiles b, b + G,
+// b + 2G, ... (G = gridDim.x, column tiles fastest).  Thread 0 keeps kStages
+// TMA tile loads in flight; all threads wait on the tile's mbarrier, compute,
+// and meet at a barrier before the stage is refilled.  Used inline in each
+// kernel so that the kernel parameters stay constant-bank operands.
+struct TileRing {
+  uint8_t* smem;
+  uint32_t bar0;
+  int ntc, ntiles;
+  const CUtensorMap* tm;
+
+  __device__ __forceinline__ void issue(int s, int tile) const {
+    const int tr0 = (tile / ntc) * kTR, tc0 = (tile % ntc) * kTC;
+    const uint32_t bar = bar0 + 8 * s;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kTileBytes) : "memory");
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+          ::"r"(smem_addr(smem + s * kTileBytes + b * kBoxBytes)), "l"(tm), "r"(tc0 + 64 * b), "r"(tr0), "r"(bar)
+          : "memory");
+  }
+
+  __device__ __forceinline__ void init(const CUtensorMap* tmap, int64_t rows, int64_t cols) {
+    extern __shared__ uint8_t smem_raw[];
+    smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    bar0 = smem_addr(smem + kStages * kTileBytes);
+    ntc = (int)((cols + kTC - 1) / kTC);
+    ntiles = ntc * (int)((rows + kTR - 1) / kTR);
+    tm = tmap;
+    if (threadIdx.x == 0) {
+      for (int s = 0; s < kStages; ++s)
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8 * s) : "memory");
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
+      for (int s = 0; s < kStages; ++s) {
+        const int t = blockIdx.x + s * gridDim.x;
+        if (t < ntiles) issue(s, t);
+      }
+    }
+  }
+
+  // Wait for the k-th tile of this CTA; false (after raising FP4Q_DEV_TIMEOUT
+  // and draining this CTA's own loads) when it did not arrive in time.
+  __device__ __forceinline__ bool wait(int k, uint32_t* status) const {
+    const int s = k % kStages;
+    const bool ok = mbar_wait_bounded(bar0 + 8 * s, (uint32_t)(k / kStages) & 1u);
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) {
+        raise_status(status, FP4Q_DEV_TIMEOUT);
+        for (int j = 0; j < kStages; ++j) {
+          const int kk = k + j, tt = blockIdx.x + kk * gridDim.x;
+          if (tt < ntiles) (void)mbar_wait_bounded(bar0 + 8 * (kk % kStages), (uint32_t)(kk / kStages) & 1u);
+        }
+      }
+      __syncthreads();
+      return false;
+    }
+    return true;
+  }
+
+  __device__ __forceinline__ TileView view(int k) const { return TileView{smem + (k % kStages) * kTileBytes}; }
+
+  // All threads are done with the k-th tile: refill its stage.
+  __device__ __forceinline__ void release(int k, int tile) const {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int nt = tile + kStages * gridDim.x;
+      if (nt < ntiles) issue(k % kStages, nt);
+    }
+  }
+};
+
 // Row-wise chunk q (0..7) of tile row r as pairs with the signs applied.
 __device__ __forceinline__ void read_row_chunk(const TileView& tv, int r, int q, const uint32_t* sgn,
                                                float2 (&P)[16]) {
@@ -331,79 +435,32 @@ __device__ __forceinline__ void read_row_chunk(const TileView& tv, int r, int q,
   }
 }
 
-// Row-wise task g (0..511) of a tile -> (row, chunk): eight consecutive tasks
-// are eight rows with distinct r & 7 of one chunk.
-__device__ __forceinline__ void row_task(int g, int& r, int& q) {
-  r = (g & 7) | ((g >> 6) << 3);
-  q = (g >> 3) & 7;
+// Column c (0..255) of the tile's 32 rows as pairs with the signs applied.
+// A word holds columns 2p (low half) and 2p+1 (high half); one byte permute
+// moves this thread's half to the top and clears the rest.
+__device__ __forceinline__ void read_col_chunk(const TileView& tv, int c, const uint32_t* sgn, float2 (&P)[16]) {
+  const uint32_t sel = (c & 1) ? 0x3244u : 0x1044u;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t a = tv.word(i, c >> 1), b = tv.word(i + 16, c >> 1);
+    P[i].x = __uint_as_float(__byte_perm(a, 0u, sel) ^ sgn[i]);
+    P[i].y = __uint_as_float(__byte_perm(b, 0u, sel) ^ sgn[i + 16]);
+  }
 }
 
-// Persistent loop over the tiles of the matrix: CTA b takes tiles b, b + G,
-// b + 2G, ... (G = gridDim.x, column tiles fastest).  Thread 0 keeps kStages
-// TMA tile loads in flight; all threads wait on the tile's mbarrier, run
-// f(tile, tr0, tc0) and meet at a barrier before the stage is refilled.
-// Returns false (after raising FP4Q_DEV_TIMEOUT and draining its own loads)
-// when a load did not arrive within the bounded wait.
-template <class F>
-__device__ __forceinline__ bool tile_loop(const CUtensorMap* tm, int64_t rows, int64_t cols, uint32_t* status,
-                                          F&& f) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t bar0 = smem_addr(smem + kStages * kTileBytes);
-  const int ntc = (int)((cols + kTC - 1) / kTC);
-  const int ntiles = ntc * (int)((rows + kTR - 1) / kTR);
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8 * s) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-  auto issue = [&](int s, int tile) {
-    const int tr0 = (tile / ntc) * kTR, tc0 = (tile % ntc) * kTC;
-    const uint32_t bar = bar0 + 8 * s;
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kTileBytes) : "memory");
-#pragma unroll
-    for (int b = 0; b < 4; ++b)
-      asm volatile(
-          "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-          ::"r"(smem_addr(smem + s * kTileBytes + b * 8192)), "l"(tm), "r"(tc0 + 64 * b), "r"(tr0), "r"(bar)
-          : "memory");
-  };
-  if (threadIdx.x == 0) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
-    for (int s = 0; s < kStages; ++s) {
-      const int t = blockIdx.x + s * gridDim.x;
-      if (t < ntiles) issue(s, t);
-    }
-  }
-  int k = 0;
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
-    const int s = k % kStages;
-    const bool ok = mbar_wait_bounded(bar0 + 8 * s, (uint32_t)(k / kStages) & 1u);
-    if (__syncthreads_or(!ok)) {
-      if (threadIdx.x == 0) {
-        raise_status(status, FP4Q_DEV_TIMEOUT);
-        for (int j = 0; j < kStages; ++j) {   // bounded drain of this CTA's own loads
-          const int kk = k + j, tt = blockIdx.x + kk * gridDim.x;
-          if (tt < ntiles) (void)mbar_wait_bounded(bar0 + 8 * (kk % kStages), (uint32_t)(kk / kStages) & 1u);
-        }
-      }
-      __syncthreads();
-      return false;
-    }
-    f(TileView{smem + s * kTileBytes}, (int64_t)(tile / ntc) * kTR, (int64_t)(tile % ntc) * kTC);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const int nt = tile + kStages * gridDim.x;
-      if (nt < ntiles) issue(s, nt);
-    }
-  }
-  return true;
+// Row-wise task t (0..255) of a tile -> (row, chunk): eight consecutive tasks
+// are eight rows with distinct r & 7 of one chunk.
+__device__ __forceinline__ void row_task(int t, int& r, int& q) {
+  r = (t & 7) | ((t >> 6) << 3);
+  q = (t >> 3) & 7;
 }
 
 // ------------------------------------------------------------ fused kernel
+// Per tile each thread quantizes one column chunk (32 rows of one column, the
+// column-wise copy) and one row chunk (32 columns of one row, the row-wise
+// copy).
 template <int GRID, int SCALE, int NH, int ROUND>
-__global__ void __launch_bounds__(kNT, 2)
+__global__ void __launch_bounds__(kNT, QUANT_MIN_CTAS)
     rht_quant_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
   const uint32_t key0 = (uint32_t)p.sr_seed, key1 = (uint32_t)(p.sr_seed >> 32);
   constexpr float kDen = 448.0f * GridK<GRID>::kQmax;
@@ -416,53 +473,41 @@ __global__ void __launch_bounds__(kNT, 2)
       if (p.want_col) *p.col.tensor_scale = S_col;
     }
   }
-  tile_loop(&tmx, p.rows, p.cols, p.status, [&](const TileView& tv, int64_t tr0, int64_t tc0) {
-    // column-wise copy: thread owns columns 2cp, 2cp+1 of tile rows 32h .. 32h+31
+  TileRing ring;
+  ring.init(&tmx, p.rows, p.cols);
+  int k = 0;
+  for (int tile = blockIdx.x; tile < ring.ntiles; tile += gridDim.x, ++k) {
+    if (!ring.wait(k, p.status)) return;
+    const TileView tv = ring.view(k);
+    const int64_t tr0 = (int64_t)(tile / ring.ntc) * kTR, tc0 = (int64_t)(tile % ring.ntc) * kTC;
     if (p.want_col) {
-      const int cp = threadIdx.x & 127, h = threadIdx.x >> 7;
-      const int64_t col = tc0 + 2 * cp, row0 = tr0 + 32 * h;
-      if (col < p.cols && row0 < p.rows) {
-        uint32_t w[32];
-#pragma unroll
-        for (int t = 0; t < 32; ++t) w[t] = tv.word(32 * h + t, cp);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float2 P[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const uint32_t a = half ? (w[i] & 0xFFFF0000u) : (w[i] << 16);
-            const uint32_t b = half ? (w[i + 16] & 0xFFFF0000u) : (w[i + 16] << 16);
-            P[i].x = __uint_as_float(a ^ p.sgn_col[i]);
-            P[i].y = __uint_as_float(b ^ p.sgn_col[i + 16]);
-          }
-          rotate_chunk<NH>(P);
-          const int64_t c = col + half;
-          ChunkOut o;
-          quantize_chunk<GRID, SCALE, ROUND>(P, S_col, (uint64_t)(c * p.rows + row0), 1u, key0, key1,
-                                             p.emit_e4m3, p.status, o);
-          store_chunk<SCALE>(p.col, c, row0, p.rows, p.sf_mma, p.emit_e4m3, o);
-        }
+      const int64_t c = tc0 + threadIdx.x;
+      if (c < p.cols && tr0 < p.rows) {
+        float2 P[16];
+        read_col_chunk(tv, threadIdx.x, p.sgn_col, P);
+        rotate_chunk<NH>(P);
+        ChunkOut o;
+        quantize_chunk<GRID, SCALE, ROUND>(P, S_col, (uint64_t)(c * p.rows + tr0), 1u, key0, key1,
+                                           p.emit_e4m3, p.status, o);
+        store_chunk<SCALE>(p.col, c, tr0, p.rows, p.sf_mma, p.emit_e4m3, o);
       }
     }
-    // row-wise copy: two (row, chunk) tasks per thread
     if (p.want_row) {
-#pragma unroll 1
-      for (int k = 0; k < (kTR * (kTC / 32)) / kNT; ++k) {
-        int r, q;
-        row_task(threadIdx.x + kNT * k, r, q);
-        const int64_t gr = tr0 + r, gc = tc0 + 32 * q;
-        if (gr < p.rows && gc < p.cols) {
-          float2 P[16];
-          read_row_chunk(tv, r, q, p.sgn_row, P);
-          rotate_chunk<NH>(P);
-          ChunkOut o;
-          quantize_chunk<GRID, SCALE, ROUND>(P, S_row, (uint64_t)(gr * p.cols + gc), 0u, key0, key1,
-                                             p.emit_e4m3, p.status, o);
-          store_chunk<SCALE>(p.row, gr, gc, p.cols, p.sf_mma, p.emit_e4m3, o);
-        }
+      int r, q;
+      row_task(threadIdx.x, r, q);
+      const int64_t gr = tr0 + r, gc = tc0 + 32 * q;
+      if (gr < p.rows && gc < p.cols) {
+        float2 P[16];
+        read_row_chunk(tv, r, q, p.sgn_row, P);
+        rotate_chunk<NH>(P);
+        ChunkOut o;
+        quantize_chunk<GRID, SCALE, ROUND>(P, S_row, (uint64_t)(gr * p.cols + gc), 0u, key0, key1,
+                                           p.emit_e4m3, p.status, o);
+        store_chunk<SCALE>(p.row, gr, gc, p.cols, p.sf_mma, p.emit_e4m3, o);
       }
     }
-  });
+    ring.release(k, tile);
+  }
 }
 
 // ------------------------------------------------------------ amax pass
@@ -471,41 +516,35 @@ __global__ void __launch_bounds__(kNT, 2)
 // atomicMax on the float bits (non-negative floats order like their bit
 // patterns).  amax[0..1] must hold 0 beforehand.
 template <int NH>
-__global__ void __launch_bounds__(kNT, 2) rotated_amax_kernel(const __grid_constant__ CUtensorMap tmx,
-                                                              const QuantParams p, float* amax) {
+__global__ void __launch_bounds__(kNT, QUANT_MIN_CTAS) rotated_amax_kernel(const __grid_constant__ CUtensorMap tmx,
+                                                                           const QuantParams p, float* amax) {
   __shared__ float red[2][kNT / 32];
   float mrow = 0.0f, mcol = 0.0f;
-  tile_loop(&tmx, p.rows, p.cols, p.status, [&](const TileView& tv, int64_t, int64_t) {
+  TileRing ring;
+  ring.init(&tmx, p.rows, p.cols);
+  int k = 0;
+  for (int tile = blockIdx.x; tile < ring.ntiles; tile += gridDim.x, ++k) {
+    if (!ring.wait(k, p.status)) return;
+    const TileView tv = ring.view(k);
     // zero-filled padding contributes |0| and cannot raise the maximum
     if (p.want_col) {
-      const int cp = threadIdx.x & 127, h = threadIdx.x >> 7;
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        float2 P[16];
+      float2 P[16];
+      read_col_chunk(tv, threadIdx.x, p.sgn_col, P);
+      rotate_chunk<NH>(P);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint32_t wa = tv.word(32 * h + i, cp), wb = tv.word(32 * h + i + 16, cp);
-          P[i].x = __uint_as_float((half ? (wa & 0xFFFF0000u) : (wa << 16)) ^ p.sgn_col[i]);
-          P[i].y = __uint_as_float((half ? (wb & 0xFFFF0000u) : (wb << 16)) ^ p.sgn_col[i + 16]);
-        }
-        rotate_chunk<NH>(P);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) mcol = absmax_nan(mcol, absmax_nan(P[i].x, P[i].y));
-      }
+      for (int i = 0; i < 16; ++i) mcol = absmax_nan(mcol, absmax_nan(P[i].x, P[i].y));
     }
     if (p.want_row) {
-#pragma unroll 1
-      for (int k = 0; k < (kTR * (kTC / 32)) / kNT; ++k) {
-        int r, q;
-        row_task(threadIdx.x + kNT * k, r, q);
-        float2 P[16];
-        read_row_chunk(tv, r, q, p.sgn_row, P);
-        rotate_chunk<NH>(P);
+      int r, q;
+      row_task(threadIdx.x, r, q);
+      float2 P[16];
+      read_row_chunk(tv, r, q, p.sgn_row, P);
+      rotate_chunk<NH>(P);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) mrow = absmax_nan(mrow, absmax_nan(P[i].x, P[i].y));
-      }
+      for (int i = 0; i < 16; ++i) mrow = absmax_nan(mrow, absmax_nan(P[i].x, P[i].y));
     }
-  });
+    ring.release(k, tile);
+  }
   mrow = fabsf(mrow);
   mcol = fabsf(mcol);
 #pragma unroll
@@ -599,70 +638,65 @@ __global__ void __launch_bounds__(256) dequant_kernel(DequantParams d) {
 // Rotation only, written back in bf16 (RNE): the first kernel of the unfused
 // rotate-then-quantize comparison.
 template <int NH>
-__global__ void __launch_bounds__(kNT, 2) rotate_bf16_kernel(const __grid_constant__ CUtensorMap tmx,
-                                                             const QuantParams p, uint16_t* y_row,
-                                                             uint16_t* y_col) {
-  tile_loop(&tmx, p.rows, p.cols, p.status, [&](const TileView& tv, int64_t tr0, int64_t tc0) {
+__global__ void __launch_bounds__(kNT, QUANT_MIN_CTAS) rotate_bf16_kernel(const __grid_constant__ CUtensorMap tmx,
+                                                                          const QuantParams p, uint16_t* y_row,
+                                                                          uint16_t* y_col) {
+  TileRing ring;
+  ring.init(&tmx, p.rows, p.cols);
+  int k = 0;
+  for (int tile = blockIdx.x; tile < ring.ntiles; tile += gridDim.x, ++k) {
+    if (!ring.wait(k, p.status)) return;
+    const TileView tv = ring.view(k);
+    const int64_t tr0 = (int64_t)(tile / ring.ntc) * kTR, tc0 = (int64_t)(tile % ring.ntc) * kTC;
     if (y_col) {
-      const int cp = threadIdx.x & 127, h = threadIdx.x >> 7;
-      const int64_t col = tc0 + 2 * cp, row0 = tr0 + 32 * h;
-      if (col < p.cols && row0 < p.rows) {
-        float2 Pa[16], Pb[16];
+      const int64_t c = tc0 + threadIdx.x;
+      if (c < p.cols && tr0 < p.rows) {
+        float2 P[16];
+        read_col_chunk(tv, threadIdx.x, p.sgn_col, P);
+        rotate_chunk<NH>(P);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const uint32_t wa = tv.word(32 * h + i, cp), wb = tv.word(32 * h + i + 16, cp);
-          Pa[i].x = __uint_as_float((wa << 16) ^ p.sgn_col[i]);
-          Pa[i].y = __uint_as_float((wb << 16) ^ p.sgn_col[i + 16]);
-          Pb[i].x = __uint_as_float((wa & 0xFFFF0000u) ^ p.sgn_col[i]);
-          Pb[i].y = __uint_as_float((wb & 0xFFFF0000u) ^ p.sgn_col[i + 16]);
-        }
-        rotate_chunk<NH>(Pa);
-        rotate_chunk<NH>(Pb);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          uint32_t* o0 = reinterpret_cast<uint32_t*>(y_col + (row0 + i) * p.cols + col);
-          uint32_t* o1 = reinterpret_cast<uint32_t*>(y_col + (row0 + i + 16) * p.cols + col);
-          *o0 = f32_to_bf16_rne(Pa[i].x) | (f32_to_bf16_rne(Pb[i].x) << 16);
-          *o1 = f32_to_bf16_rne(Pa[i].y) | (f32_to_bf16_rne(Pb[i].y) << 16);
+          y_col[(tr0 + i) * p.cols + c] = (uint16_t)f32_to_bf16_rne(P[i].x);
+          y_col[(tr0 + i + 16) * p.cols + c] = (uint16_t)f32_to_bf16_rne(P[i].y);
         }
       }
     }
     if (y_row) {
-#pragma unroll 1
-      for (int k = 0; k < (kTR * (kTC / 32)) / kNT; ++k) {
-        int r, q;
-        row_task(threadIdx.x + kNT * k, r, q);
-        const int64_t gr = tr0 + r, gc = tc0 + 32 * q;
-        if (gr < p.rows && gc < p.cols) {
-          float2 P[16];
-          read_row_chunk(tv, r, q, p.sgn_row, P);
-          rotate_chunk<NH>(P);
-          uint32_t o[16];
+      int r, q;
+      row_task(threadIdx.x, r, q);
+      const int64_t gr = tr0 + r, gc = tc0 + 32 * q;
+      if (gr < p.rows && gc < p.cols) {
+        float2 P[16];
+        read_row_chunk(tv, r, q, p.sgn_row, P);
+        rotate_chunk<NH>(P);
+        uint32_t o[16];
 #pragma unroll
-          for (int k2 = 0; k2 < 8; ++k2) {
-            o[k2] = f32_to_bf16_rne(P[2 * k2].x) | (f32_to_bf16_rne(P[2 * k2 + 1].x) << 16);
-            o[k2 + 8] = f32_to_bf16_rne(P[2 * k2].y) | (f32_to_bf16_rne(P[2 * k2 + 1].y) << 16);
-          }
-          uint4* dst = reinterpret_cast<uint4*>(y_row + gr * p.cols + gc);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        for (int k2 = 0; k2 < 8; ++k2) {
+          o[k2] = f32_to_bf16_rne(P[2 * k2].x) | (f32_to_bf16_rne(P[2 * k2 + 1].x) << 16);
+          o[k2 + 8] = f32_to_bf16_rne(P[2 * k2].y) | (f32_to_bf16_rne(P[2 * k2 + 1].y) << 16);
         }
+        uint4* dst = reinterpret_cast<uint4*>(y_row + gr * p.cols + gc);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
       }
     }
-  });
+    ring.release(k, tile);
+  }
 }
 
 // ------------------------------------------------------------ launchers
-// The input's tensor map: bf16 [rows][cols] with row stride ld, 64 x 64 boxes,
-// 128-byte swizzle, zero fill outside the matrix.
+// The input's tensor map: bf16 [rows][cols] with row stride ld, boxes of kTR
+// rows x 64 columns (kBoxBytes, one ring slot each), 128-byte swizzle, zero
+// fill outside the matrix.
 static bool input_map(const QuantParams& p, CUtensorMap* m) {
+  static_assert(kTR * 64 * 2 == kBoxBytes, "a TMA box must fill exactly one ring slot");
   return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.x, (uint64_t)p.cols, (uint64_t)p.rows,
-                        (uint64_t)p.ld * 2u, 64u, 64u, CU_TENSOR_MAP_SWIZZLE_128B);
+                        (uint64_t)p.ld * 2u, 64u, (uint32_t)kTR, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 static unsigned persistent_grid(const QuantParams& p) {
   const int64_t ntiles = ((p.cols + kTC - 1) / kTC) * ((p.rows + kTR - 1) / kTR);
-  const int64_t g = 2 * (int64_t)num_sms();
+  const int64_t g = QUANT_MIN_CTAS * (int64_t)num_sms();
   return (unsigned)(ntiles < g ? ntiles : g);
 }
 
@@ -707,6 +741,10 @@ cudaError_t launch_rht_quant(const QuantParams& p, int grid_kind, int scale, int
     return scale == FP4Q_SCALE_NV ? launch_quant_nh<FP4Q_GRID_E2M1, FP4Q_SCALE_NV>(m, p, nh, round, s)
                                   : launch_quant_nh<FP4Q_GRID_E2M1, FP4Q_SCALE_MX>(m, p, nh, round, s);
   }
+  if (grid_kind == FP4Q_GRID_E2M1_R4) {
+    return scale == FP4Q_SCALE_NV ? launch_quant_nh<FP4Q_GRID_E2M1_R4, FP4Q_SCALE_NV>(m, p, nh, round, s)
+                                  : launch_quant_nh<FP4Q_GRID_E2M1_R4, FP4Q_SCALE_MX>(m, p, nh, round, s);
+  }
   return scale == FP4Q_SCALE_NV ? launch_quant_nh<FP4Q_GRID_E1M2, FP4Q_SCALE_NV>(m, p, nh, round, s)
                                 : launch_quant_nh<FP4Q_GRID_E1M2, FP4Q_SCALE_MX>(m, p, nh, round, s);
 }
@@ -744,7 +782,7 @@ static void launch_deq_nh(const DequantParams& d, int nh, unsigned nb, cudaStrea
 cudaError_t launch_dequant(const DequantParams& d, int grid_kind, int scale, int nh, cudaStream_t s) {
   const int64_t nchunks = d.rows * (d.cols >> 5);
   const unsigned nb = (unsigned)((nchunks + 255) / 256);
-  if (grid_kind == FP4Q_GRID_E2M1) {
+  if (grid_kind != FP4Q_GRID_E1M2) {   // the capped grid decodes with the E2M1 table
     if (scale == FP4Q_SCALE_NV) launch_deq_nh<FP4Q_GRID_E2M1, FP4Q_SCALE_NV>(d, nh, nb, s);
     else launch_deq_nh<FP4Q_GRID_E2M1, FP4Q_SCALE_MX>(d, nh, nb, s);
   } else {

@@ -20,7 +20,7 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "fp4q.h")
 # enums (values fixed by include/fp4q.h)
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIGNMENT, ERR_CUDA, ERR_WORKSPACE = range(6)
 DEV_NONFINITE, DEV_TIMEOUT = 0x1, 0x2
-GRID_E2M1, GRID_E1M2 = 0, 1
+GRID_E2M1, GRID_E1M2, GRID_E2M1_R4 = 0, 1, 2
 SCALE_MX, SCALE_NV = 0, 1
 ROT_NONE, ROT_H16, ROT_H32 = 0, 16, 32
 RTNE, SR = 0, 1
@@ -266,10 +266,16 @@ def bias_stats(ref: torch.Tensor, approx: torch.Tensor, codes: torch.Tensor | No
 
 
 def hadamard_rotate_bf16(x: torch.Tensor, rot: int, sign_mask_row: int = 0, sign_mask_col: int = 0,
-                         want_row: bool = True, want_col: bool = True, stream=None):
+                         want_row: bool = True, want_col: bool = True, y_row=None, y_col=None, stream=None):
     R, C = x.shape
-    y_row = torch.empty((R, C), dtype=torch.bfloat16, device=x.device) if want_row else None
-    y_col = torch.empty((R, C), dtype=torch.bfloat16, device=x.device) if want_col else None
+    if want_row and y_row is None:
+        y_row = torch.empty((R, C), dtype=torch.bfloat16, device=x.device)
+    if want_col and y_col is None:
+        y_col = torch.empty((R, C), dtype=torch.bfloat16, device=x.device)
+    if not want_row:
+        y_row = None
+    if not want_col:
+        y_col = None
     _check("fp4q_hadamard_rotate_bf16", lib().fp4q_hadamard_rotate_bf16(
         x.data_ptr(), R, C, x.stride(0), rot, sign_mask_row & 0xFFFFFFFF, sign_mask_col & 0xFFFFFFFF,
         _p(y_row), _p(y_col), _stream(stream)))

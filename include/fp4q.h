@@ -53,13 +53,15 @@ typedef enum {
 
 /* 4-bit element grids ([SB] Declaracao do Problema; Metodologia 2):
  * E2M1 magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6}; E1M2 magnitudes {k/4, k = 0..7}.
+ * E2M1_R4 ([SB] Resultados, ablation of a range-restricted E2M1): E2M1 with
+ * its maximum capped at 4 (codes 0..6, E2M1 bit patterns, e_max = 1).
  * A code is (sign << 3) | k. */
-enum { FP4Q_GRID_E2M1 = 0, FP4Q_GRID_E1M2 = 1 };
+enum { FP4Q_GRID_E2M1 = 0, FP4Q_GRID_E1M2 = 1, FP4Q_GRID_E2M1_R4 = 2 };
 
 /* Block scaling.
  * MX ([HTX] Que es MXFP4?): 32-element blocks sharing one E8M0 exponent,
  *    e = clamp(floor(log2 amax) - e_max, -127, 127), byte = e + 127,
- *    e_max = 2 (E2M1) or 0 (E1M2); element v = y * 2^-e.
+ *    e_max = 2 (E2M1), 0 (E1M2) or 1 (E2M1_R4); element v = y * 2^-e.
  * NV (NVFP4-style, named in [SB] Declaracao do Problema): 16-element blocks,
  *    fp32 tensor scale S_t = G / (448 q_max) from the global amax G of the
  *    rotated copy, E4M3 block scale sb = E4M3_rtne_sat(fl(fl(amax/q_max)/S_t)),
@@ -175,7 +177,7 @@ int32_t fp4q_dequantize(const fp4q_operand* q, int64_t rows, int64_t cols,
  *  Wgrad dW = dY^T X, each written with K-major operands).
  *  A        M x K copy (codes; scales in FP4Q_SF_MMA layout; e4m3 for E1M2)
  *  B        N x K copy, same form
- *  grid, scale   the operands' recipe.  E2M1+MX runs kind::mxf4, E2M1+NV runs
+ *  grid, scale   the operands' recipe (E2M1_R4 runs as E2M1).  E2M1+MX runs kind::mxf4, E2M1+NV runs
  *           kind::mxf4nvf4 with E4M3 scales, E1M2+MX runs kind::mxf8f6f4 on the
  *           E4M3 bytes (E1M2 levels are exact in E4M3).  E1M2+NV is
  *           FP4Q_ERR_UNSUPPORTED.  alpha_g = S_t(A) * S_t(B) for NV, else 1.

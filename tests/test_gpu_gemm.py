@@ -70,7 +70,7 @@ def check_gemm(fq, orc, a_bits, b_bits, grid, scale, rot=16, mask=0):
     return rel
 
 
-@pytest.mark.parametrize("grid,scale", [(0, 0), (0, 1), (1, 0)])
+@pytest.mark.parametrize("grid,scale", [(0, 0), (0, 1), (1, 0), (2, 0), (2, 1)])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 256), (256, 384, 512), (128, 128, 640), (384, 256, 1152)])
 def test_gemm_small(fq, orc, grid, scale, M, N, K):
     a = synth.normal_channel_outliers(M, K, M + K, 4, 20.0)

@@ -71,7 +71,7 @@ def run_case(fq, orc, x_bits, cfg, given=None):
 SHAPES = [(96, 800), (160, 288), (64, 256), (32, 32)]   # several tiles, ragged tails, a single chunk
 
 
-@pytest.mark.parametrize("grid,scale,rot,rnd", list(itertools.product([0, 1], [0, 1], [0, 16, 32], [0, 1])))
+@pytest.mark.parametrize("grid,scale,rot,rnd", list(itertools.product([0, 1, 2], [0, 1], [0, 16, 32], [0, 1])))
 def test_quantize_all_modes_small(fq, orc, grid, scale, rot, rnd):
     for si, (R, C) in enumerate(SHAPES):
         x = synth.special_values(R, C, 100 + si) if si % 2 else synth.normal_point_outliers(R, C, 200 + si)
@@ -83,7 +83,7 @@ def test_quantize_all_modes_small(fq, orc, grid, scale, rot, rnd):
             run_case(fq, orc, x, cfg)
 
 
-@pytest.mark.parametrize("grid,scale", [(0, 0), (1, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("grid,scale", [(0, 0), (1, 0), (0, 1), (1, 1), (2, 0), (2, 1)])
 def test_quantize_mma_scale_layout(fq, orc, grid, scale):
     x = synth.normal_channel_outliers(256, 384, 7)
     cfg = fq.Config(grid=grid, scale=scale, rot=16, sign_mask_row=0x1234, sign_mask_col=0xBEEF,
@@ -139,7 +139,7 @@ def test_empty_and_nonfinite(fq, orc):
         assert st.item() & fq.DEV_NONFINITE
 
 
-@pytest.mark.parametrize("grid,scale,rot", [(0, 0, 16), (1, 0, 32), (0, 1, 16), (1, 1, 32), (0, 0, 0)])
+@pytest.mark.parametrize("grid,scale,rot", [(0, 0, 16), (1, 0, 32), (0, 1, 16), (1, 1, 32), (0, 0, 0), (2, 0, 16), (2, 1, 32)])
 def test_dequantize_exact(fq, orc, grid, scale, rot):
     x = synth.special_values(64, 256, 17)
     cfg = fq.Config(grid=grid, scale=scale, rot=rot, sign_mask_row=0x0F0F, sign_mask_col=0x3333)
