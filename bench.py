@@ -271,8 +271,7 @@ def run_ours(args, world, rank, local):
     x_launch = statistics.mean(kq["x"])
     x_bytes = MX_BYTES_PER_ELEM * TOKENS * D_IN
     x_achieved = x_bytes / x_launch / 1e9
-    traffic = json.load(open(os.path.join(ROOT, "profiles", "traffic.json"))) if os.path.exists(
-        os.path.join(ROOT, "profiles", "traffic.json")) else {}
+    traffic = read_traffic()
     dominant_gemm = sum(g_times) >= sum(q_times)
     roof_gemm = {"kernel": "bs_gemm_kernel<mxf4> (tcgen05)", "bound": "tensor", "achieved": round(g_achieved, 1),
                  "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(g_achieved / fp4_peak, 4),
@@ -305,9 +304,117 @@ def run_ours(args, world, rank, local):
         "clocks": clk,
         "wall_s_timed": round(wall, 4),
     }
+    if not args.no_configs:
+        del hX, hW, hdY, hY, hdX, hdW
+        line["quantizer_configs"] = quant_configs(dev, stream, flush)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
     return line
+
+
+def read_traffic() -> dict:
+    """DRAM bytes per launch measured by ncu (profiles/dram_traffic.txt: 'key bytes' lines)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    out = {}
+    if os.path.exists(path):
+        for line in open(path):
+            parts = line.split()
+            if len(parts) == 2 and not line.startswith("#"):
+                out[parts[0]] = int(parts[1])
+    return out
+
+
+# ------------------------------------------------------------------ quantizer configurations
+def quant_configs(dev, stream, flush, reps: int = 20) -> dict:
+    """The quantizer alone on each workload shape: microseconds per call (median
+    of `reps`, L2 flushed before each, outside the events) and GB/s of
+    algorithmic bytes; the fused call against the same call without rotation
+    (plain) and against a separate rotation kernel followed by plain
+    quantization of each rotated copy (unfused)."""
+    import torch
+
+    from fp4_microscaled_quantization_gb300 import fp4q, synth
+
+    def timed(fn):
+        ts = []
+        for i in range(reps + 2):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            if i >= 2:
+                ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(ts)
+
+    out = {}
+
+    def entry(name, us, nbytes):
+        out[name] = {"us": round(us, 2), "gb_s": round(nbytes / us / 1e3, 1) if nbytes else None}
+
+    def q_bytes(R, C, b, copies):
+        return 2.0 * R * C + copies * R * C * (0.5 + 1.0 / b)
+
+    # tiny: X 256x512, row-wise copy only, random H16 (launch-bound; microseconds only)
+    x = synth.as_torch(synth.tiny_x()).to(dev)
+    m = fp4q.sign_mask_from_seed(1001, 16)
+    for g, gname in ((0, "e2m1"), (1, "e1m2")):
+        cfg = fp4q.Config(grid=g, rot=16, sign_mask_row=m, want_col=False)
+        ro, _ = fp4q.rht_quantize(x, cfg, stream=stream)
+        entry(f"tiny_256x512_row_{gname}", timed(lambda: fp4q.rht_quantize(x, cfg, ro, stream=stream)), 0)
+    # activations: X 8192x4096 both copies, deterministic H16, MX; plain and unfused arms
+    x = synth.as_torch(synth.act_x()).to(dev)
+    R, C = x.shape
+    for g, gname in ((0, "e2m1"), (1, "e1m2"), (2, "e2m1_cap4")):
+        cfg = fp4q.Config(grid=g, rot=16)
+        ro, co = fp4q.rht_quantize(x, cfg, stream=stream)
+        entry(f"act_8192x4096_{gname}_h16", timed(lambda: fp4q.rht_quantize(x, cfg, ro, co, stream=stream)),
+              q_bytes(R, C, 32, 2))
+    cfg = fp4q.Config(grid=0, rot=0)
+    ro, co = fp4q.rht_quantize(x, cfg, stream=stream)
+    plain = timed(lambda: fp4q.rht_quantize(x, cfg, ro, co, stream=stream))
+    entry("act_8192x4096_e2m1_plain", plain, q_bytes(R, C, 32, 2))
+    yr = torch.empty_like(x)
+    yc = torch.empty_like(x)
+    cr = fp4q.Config(grid=0, rot=0, want_col=False)
+    cc = fp4q.Config(grid=0, rot=0, want_row=False)
+
+    def unfused():
+        fp4q.hadamard_rotate_bf16(x, 16, 0, 0, y_row=yr, y_col=yc, stream=stream)
+        fp4q.rht_quantize(yr, cr, ro, None, stream=stream)
+        fp4q.rht_quantize(yc, cc, None, co, stream=stream)
+    unf = timed(unfused)
+    entry("act_8192x4096_e2m1_unfused", unf, q_bytes(R, C, 32, 2))
+    fused = out["act_8192x4096_e2m1_h16"]["us"]
+    out["fusion_ratio_fused_over_plain"] = round(fused / plain, 3)
+    out["fusion_ratio_unfused_over_plain"] = round(unf / plain, 3)
+    del x, yr, yc
+    # gradients: dY 8192x14336, E1M2, random H16, stochastic rounding, both copies
+    x = synth.as_torch(synth.grad_dy()).to(dev)
+    R, C = x.shape
+    cfg = fp4q.Config(grid=1, rot=16, round=fp4q.SR, sign_mask_row=fp4q.sign_mask_from_seed(1003, 16),
+                      sign_mask_col=fp4q.sign_mask_from_seed(1004, 16), sr_seed=1004)
+    ro, co = fp4q.rht_quantize(x, cfg, stream=stream)
+    entry("grad_8192x14336_e1m2_sr_h16", timed(lambda: fp4q.rht_quantize(x, cfg, ro, co, stream=stream)),
+          q_bytes(R, C, 32, 2))
+    del x, ro, co
+    # weights: W 14336x4096, deterministic H32, NVFP4-style scales, one and two passes
+    x = synth.as_torch(synth.weight_w()).to(dev)
+    R, C = x.shape
+    for g, gname in ((0, "e2m1"), (1, "e1m2")):
+        cfg = fp4q.Config(grid=g, scale=fp4q.SCALE_NV, rot=32)
+        ro, co = fp4q.rht_quantize(x, cfg, stream=stream)
+        ws = torch.empty(max(1, fp4q.workspace_bytes(R, C, cfg)), dtype=torch.uint8, device=dev)
+        entry(f"weight_14336x4096_{gname}_nv_h32_two_pass",
+              timed(lambda: fp4q.rht_quantize(x, cfg, ro, co, workspace=ws, stream=stream)),
+              q_bytes(R, C, 16, 2) + 2.0 * R * C)
+        amax = fp4q.rotated_amax(x, cfg, stream=stream)
+        cfg1 = fp4q.Config(grid=g, scale=fp4q.SCALE_NV, rot=32, global_amax=amax)
+        entry(f"weight_14336x4096_{gname}_nv_h32_one_pass",
+              timed(lambda: fp4q.rht_quantize(x, cfg1, ro, co, stream=stream)), q_bytes(R, C, 16, 2))
+    torch.cuda.synchronize(dev)
+    return out
 
 
 # ------------------------------------------------------------------ oracle arm
@@ -381,6 +488,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-shape quantizer timings")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

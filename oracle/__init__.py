@@ -9,7 +9,7 @@ numpy's fp64 matrix product as a library step.
 
 Parity status of each function (pins live in tests/test_oracle_*.py):
   grid tables, E4M3 codec, Philox4x32-10, rotation, RTNE, SR, MX and NV
-  scales, dequantize, GEMM entries, bias sums -- pinned.
+  scales, dequantize, GEMM entries, bias sums, effective bucket ratio -- pinned.
 """
 from __future__ import annotations
 
@@ -234,3 +234,25 @@ def bias_stats(ref: np.ndarray, approx: np.ndarray, codes: np.ndarray | None = N
     alpha = s_ra / s_ref2 if s_ref2 > 0 else float("nan")
     shrink = s_absdiff / s_absref if s_absref > 0 else float("nan")
     return {"sums": sums, "hist": hist, "n": r.size, "sqnr_db": sqnr, "alpha": alpha, "shrinkage": shrink}
+
+
+def effective_bucket_ratio(hist16, grid: int) -> float:
+    """Effective number of magnitude levels used, over the levels the grid can
+    produce ("Repensando o Vies de Encolhimento", Resultados, Diagnosticos de
+    Quantizacao e GEMM, names the ratio without a formula).  Reading: fold the
+    16-code histogram onto the 8 magnitudes (code & 7), take the Shannon
+    entropy H in nats of that distribution, and return exp(H) / L with L = 8
+    (7 for the grid capped at 4, which has no code 7)."""
+    counts = [0.0] * 8
+    for code in range(16):
+        counts[code & 7] += float(hist16[code])
+    total = sum(counts)
+    if total == 0:
+        return float("nan")
+    H = 0.0
+    for c in counts:
+        if c > 0:
+            p = c / total
+            H -= p * np.log(p)
+    L = 7 if grid == GRID_E2M1_R4 else 8
+    return float(np.exp(H) / L)

@@ -5,6 +5,7 @@ and the hand-computed statistics fixture."""
 import os
 
 import numpy as np
+import pytest
 
 from fp4_microscaled_quantization_gb300 import synth
 
@@ -101,3 +102,36 @@ def test_e2m1_attenuates_more_than_e1m2_after_rotation(orc):
         out[grid] = orc.bias_stats(y, d)
     print({g: (round(v["alpha"], 5), round(v["shrinkage"], 5), round(v["sqnr_db"], 3)) for g, v in out.items()})
     assert out[0]["alpha"] < 1.0
+
+
+def test_effective_bucket_ratio_closed_forms(orc):
+    """exp(entropy)/levels: 1 for a uniform use of every level, 1/L for a single
+    level, the sign folded away, and the two-level closed form."""
+    uni = np.zeros(16)
+    uni[:8] = 10
+    assert orc.effective_bucket_ratio(uni, orc.GRID_E2M1) == pytest.approx(1.0, abs=1e-15)
+    one = np.zeros(16)
+    one[3], one[11] = 5, 7                     # +level 3 and -level 3: one magnitude
+    assert orc.effective_bucket_ratio(one, orc.GRID_E1M2) == pytest.approx(1 / 8, abs=1e-15)
+    two = np.zeros(16)
+    two[1], two[12] = 1, 3                     # p = (1/4, 3/4) over levels 1 and 4
+    H = -(0.25 * np.log(0.25) + 0.75 * np.log(0.75))
+    assert orc.effective_bucket_ratio(two, orc.GRID_E2M1) == pytest.approx(np.exp(H) / 8, rel=1e-14)
+    cap = np.zeros(16)
+    cap[:7] = 4                                 # every level the capped grid can make
+    assert orc.effective_bucket_ratio(cap, orc.GRID_E2M1_R4) == pytest.approx(1.0, abs=1e-15)
+    assert np.isnan(orc.effective_bucket_ratio(np.zeros(16), orc.GRID_E2M1))
+
+
+def test_effective_bucket_ratio_of_quantized_uniform_data(orc):
+    """Data spread evenly over the E1M2 grid's bins (every block holding one
+    value at the top so that the scale is 2^0) fills all 8 levels equally."""
+    R, C = 32, 256
+    lv = orc.grid_levels(orc.GRID_E1M2)
+    vals = np.tile(np.repeat(lv, 4), (R, 1)).astype(np.float32)     # 32 values per block, 4 per level
+    bits = (vals.view(np.uint32) >> 16).astype(np.uint16)            # exact in bf16
+    q = orc.quantize(bits, 0, orc.GRID_E1M2, orc.SCALE_MX, 0)
+    st = orc.bias_stats(vals.ravel(), orc.dequantize(q["codes"], q["scales"], 0, orc.GRID_E1M2, 0).ravel(),
+                        q["codes"])
+    assert st["sqnr_db"] == float("inf")
+    assert orc.effective_bucket_ratio(st["hist"], orc.GRID_E1M2) == pytest.approx(1.0, abs=1e-15)
