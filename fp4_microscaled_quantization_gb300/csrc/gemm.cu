@@ -9,19 +9,38 @@
 //   E1M2 + MX                    -> kind::mxf8f6f4 on the E4M3 byte copies
 //                                   (every E1M2 level k/4 is exact in E4M3)
 //
-// Structure (persistent, one CTA per SM walking 128 x 256 output tiles, 192
-// threads):
+// Structure (persistent, 320 threads per CTA; a single CTA per 128 x 256
+// output tile, or a pair of CTAs per 256 x 256 tile, see the kernel):
 //   warp 0      TMA producer: A/B tiles (128-byte swizzled K-major rows) by
-//               cp.async.bulk.tensor, scale-factor chunks by cp.async.bulk,
-//               into a 4-stage ring guarded by full/empty mbarriers.
-//   warp 1      owns the TMEM allocation; one lane copies each stage's scale
-//               factors to TMEM (tcgen05.cp 32x128b.warpx4) and issues the
-//               MMAs, then tcgen05.commit frees the stage.
-//   warps 2-5   epilogue: TMEM -> registers (tcgen05.ld), alpha, bf16/fp32
-//               stores; TMEM is released before the global stores so the
-//               next tile's MMAs overlap them.
+//               cp.async.bulk.tensor and the compact 512-byte scale chunks by
+//               cp.async.bulk, into a ring of stages guarded by mbarriers.
+//   warp 1      owns the TMEM allocation; one lane issues the MMAs of a stage
+//               once its operands and scales are in place, and tcgen05.commit
+//               frees the stage.
+//   warps 2-5   epilogue: TMEM -> registers (tcgen05.ld), alpha, bf16/fp32,
+//               then a swizzled shared-memory box stored by TMA
+//               (cp.async.bulk.tensor, bulk groups).  The accumulator is
+//               released before the stores so the next tile's MMAs overlap
+//               them.
+//   warps 6-9   scale writers, one per TMEM lane quarter: per stage they read
+//               the compact chunks from shared memory and write them to TMEM
+//               with tcgen05.st, then signal the MMA lane.
+//
+// Scale factors in TMEM.  Sub-partition q of the tensor core (accumulator
+// rows 32q..32q+31) reads its scales from TMEM lane quarter q: for A, row
+// 32q+i at lane 32q+i, column sfa + q; for B (N = 256), row n at lane
+// 32q + (n % 32), column sfb + n / 32, in every quarter.  Row i of a compact
+// chunk (16 bytes) holds rows i, 32+i, 64+i, 96+i of its 128-row group, one
+// 32-bit cell each, so lane i of every quarter stores row i of two chunks as
+// 8 consecutive columns: for B the two row groups of one K chunk (columns
+// sfb + 0..7), for A two consecutive K chunks (chunk c at sfa + 4c + 0..3, of
+// which quarter q reads cell q).  Writing the scales from registers keeps the
+// tensor pipe free of scale copies (tcgen05.cp), which cost it 15-60 cycles
+// each, and needs no shared-memory staging.
+//
 // Every mbarrier wait is bounded (about 2 s of %globaltimer); on expiry the
-// CTA raises FP4Q_DEV_TIMEOUT, stops issuing work, frees its TMEM and exits.
+// CTA raises FP4Q_DEV_TIMEOUT, stops issuing work, waits (bounded) for its
+// own tensor-core work to drain, frees its TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -31,40 +50,45 @@
 #include "../../include/fp4q.h"
 #include "fp4q_dev.cuh"
 #include "fp4q_internal.h"
-
-#ifndef FP4Q_GEMM_PAIR
-#define FP4Q_GEMM_PAIR 0
-#endif
+#include "quant_core.cuh"
 
 namespace fp4q {
 namespace {
 
 enum { KIND_MXF4 = 0, KIND_NVF4 = 1, KIND_F8 = 2 };
 
-constexpr int BM = 128;              // tile rows (TMEM lanes)
+constexpr int BM = 128;              // accumulator rows per CTA (TMEM lanes)
 constexpr int BN = 256;              // tile columns (MMA N)
 constexpr int KROW = 128;            // bytes of one operand row per K-tile (one 128B swizzle span)
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * KROW;   // 16 KB
-constexpr int B_BYTES = BN * KROW;   // 32 KB
-constexpr int SFA_OFF = A_BYTES + B_BYTES;
-constexpr int SFB_OFF = SFA_OFF + 4 * 512;
-constexpr int STAGE_BYTES = SFB_OFF + 8 * 512;   // 55296, a multiple of 1024
-constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 320;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t ACC_COL = 0;                   // accumulator columns [0, 256)
-constexpr uint32_t SF_COL0 = 256;                 // 48 scale-factor columns per stage after it
-constexpr uint32_t SF_COLS_PER_STAGE = 48;
+constexpr uint32_t ACC_COL = 0;      // accumulator columns [0, 256); scale columns after it
+constexpr int STG_BYTES = 4096;      // one epilogue store box (32 rows x 128 bytes)
 
-template <int KIND>
+template <int KIND, bool PAIR>
 struct KindK {
-  // chunks = groups of 4 consecutive scale bytes of one 128-row group
-  static constexpr int kChunksPerTile = KIND == KIND_MXF4 ? 2 : (KIND == KIND_NVF4 ? 4 : 1);
+  // chunks = 512-byte groups of 4 consecutive scale bytes of one 128-row group
+  static constexpr int kChunks = KIND == KIND_MXF4 ? 2 : (KIND == KIND_NVF4 ? 4 : 1);   // per K-tile
   static constexpr int kElemsPerTile = KIND == KIND_F8 ? 128 : 256;
   static constexpr int kMmaK = KIND == KIND_F8 ? 32 : 64;
   static constexpr int kBlock = KIND == KIND_NVF4 ? 16 : 32;
+  // B rows this CTA loads per tile: all 256, or its half of the pair's 256
+  static constexpr int kBRows = PAIR ? 128 : 256;
+  static constexpr int kBBytes = kBRows * KROW;
+  // compact chunks in a stage: A (kChunks), B row group 0 (kChunks), B row group 1 (kChunks)
+  static constexpr int kCompact = 3 * kChunks * 512;
+  // TMEM scale columns per stage: A 8 per two chunks (F8: 4 for its one chunk), B 8 per chunk
+  static constexpr int kSfColsA = KIND == KIND_F8 ? 4 : 4 * kChunks;
+  static constexpr int kSfColsB = 8 * kChunks;
+  static constexpr int kStage = (A_BYTES + kBBytes + kCompact + 1023) / 1024 * 1024;
+  static constexpr int kStagesMax = (232448 - 1280 - 4 * STG_BYTES) / kStage;
+  static constexpr int kStages = kStagesMax > 6 ? 6 : kStagesMax;
+  static constexpr int kBarOff = kStages * kStage + 4 * STG_BYTES;   // stages, then one store box per epilogue warp
+  static constexpr int kSmem = kBarOff + 256 + 1024;                 // + barriers + alignment slack
+  static_assert(kStages >= 3, "pipeline depth");
+  static_assert(kSmem <= 232448, "shared memory");
+  static_assert(ACC_COL + BN + kStages * (kSfColsA + kSfColsB) <= TMEM_COLS, "tensor memory");
 };
 
 struct GemmParams {
@@ -72,10 +96,17 @@ struct GemmParams {
   const uint8_t* sfb;     // MMA scale layout of B (N x K/b)
   const float* ts_a;      // NV tensor scales (or null)
   const float* ts_b;
-  uint16_t* d_bf16;
-  float* d_f32;
   uint32_t* status;
   int32_t M, N, K;
+  int32_t want_bf16, want_f32;
+  // fused output quantization (the kernels with QG >= 0): the row-wise copy of
+  // bf16(D) as fp4q_rht_quantize would make it from the stored bf16 D
+  uint8_t* q_codes;       // M x N/2
+  uint8_t* q_scales;      // M x N/32 E8M0 bytes, plain or MMA layout
+  uint8_t* q_e4m3;        // optional M x N E4M3 bytes
+  uint64_t q_seed;        // stochastic rounding
+  int32_t q_nh, q_sf_mma;
+  uint32_t q_sgn[32];     // sign words of a 32-element chunk (bit 31 = negate)
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -89,6 +120,9 @@ __device__ __forceinline__ uint64_t globaltimer() {
 }
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
@@ -108,7 +142,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   uint64_t t0 = 0;
   for (uint32_t i = 0;; ++i) {
     if (mbar_try(bar, parity)) return true;
-    if ((i & 255u) == 255u) {
+    if ((i & 63u) == 63u) {
       if (*abort_flag) return false;
       const uint64_t now = globaltimer();
       if (t0 == 0) t0 = now;
@@ -122,6 +156,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       ::"r"(dst), "l"(tm), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, int32_t x, int32_t y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+               ::"l"(tm), "r"(x), "r"(y), "r"(src)
+               : "memory");
 }
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
@@ -139,12 +178,7 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
 }
 // K-major operand rows of 128 bytes, 128B swizzle, 8-row groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t op_desc(uint32_t saddr) { return sdesc(saddr, 16, 1024, 2); }
-// A 32-row x 16-byte scale chunk (no swizzle, 8-row core matrices 128 bytes apart).
-__device__ __forceinline__ uint64_t sf_desc(uint32_t saddr) { return sdesc(saddr, 16, 128, 0); }
 
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t desc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
-}
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
@@ -185,11 +219,34 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// This warp's TMEM lane quarter, 8 (4) consecutive 32-bit columns from taddr.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, uint4 a, uint4 b) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               ::"r"(taddr), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint4 a) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
+               ::"r"(taddr), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w)
+               : "memory");
+}
+// 16-byte row i of a compact chunk (rows 0..31 of the 512-byte chunk).
+__device__ __forceinline__ uint4 chunk_row(uint32_t chunk, int i) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(chunk + 16u * (uint32_t)i));
+  return v;
+}
+__device__ __forceinline__ void st_shared16(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
 
 // Instruction descriptor of the block-scaled kinds: B scale id in bits 4-5,
 // A/B element types in 7-9 / 10-12, K-major A and B, N >> 3 in 17-22, scale
 // type in 23 (1 = E8M0, 0 = E4M3), M >> 4 in 24-28, A scale id in 29-30.
-template <int KIND, int MM = BM>
+template <int KIND, int MM>
 __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
   constexpr uint32_t ty = KIND == KIND_F8 ? 0u : 1u;   // E4M3 (f8f6f4) or E2M1 (mxf4 kinds)
   constexpr uint32_t sfmt = KIND == KIND_NVF4 ? 0u : 1u;
@@ -197,271 +254,13 @@ __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
          ((uint32_t)(MM >> 4) << 24) | (sf_id << 29);
 }
 
-// ------------------------------------------------------------ the kernel
-// Persistent: CTA b owns tiles b, b + G, b + 2G, ... (G = gridDim.x), tile id
-// -> (m block = id / n_blocks, n block = id % n_blocks).  The producer and
-// the MMA issuer stream through every (tile, K-tile) pair of the CTA without
-// draining the ring between tiles.  The accumulator is single-buffered: the
-// epilogue pulls a finished tile out of TMEM (as packed bf16 when only bf16 is
-// wanted), releases TMEM through acc_empty, and only then writes global
-// memory, so the next tile's MMAs overlap those stores.
-template <int KIND>
-__global__ void __launch_bounds__(NTHREADS, 1)
-    bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmParams p) {
-  using KK = KindK<KIND>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar_full = sbase + BAR_OFF;          // STAGES x 8 bytes
-  const uint32_t bar_empty = bar_full + 8 * STAGES;   // STAGES x 8 bytes
-  const uint32_t bar_acc_full = bar_empty + 8 * STAGES;
-  const uint32_t bar_acc_empty = bar_acc_full + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + BAR_OFF + 16 * STAGES + 16);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + BAR_OFF + 16 * STAGES + 24);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_blocks = (p.N + BN - 1) / BN;
-  const int n_tiles = (p.M / BM) * n_blocks;
-  const int num_kt = (p.K + KK::kElemsPerTile - 1) / KK::kElemsPerTile;
-  const int nq = p.K / KK::kBlock / 4;   // scale chunks per 128-row group
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
-    }
-    mbar_init(bar_acc_full, 1);
-    mbar_init(bar_acc_empty, 4);   // one arrival per epilogue warp
-    *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- producer
-      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
-      uint32_t it = 0;
-      for (int tile = blockIdx.x; tile < n_tiles && !*abort_flag; tile += gridDim.x) {
-        const int m0 = (tile / n_blocks) * BM, n0 = (tile % n_blocks) * BN;
-        const bool rg1 = (n0 + 128) < p.N;
-        for (int kt = 0; kt < num_kt; ++kt, ++it) {
-          const int s = (int)(it % STAGES);
-          const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag)) {
-            *abort_flag = 1;
-            raise_status(p.status, FP4Q_DEV_TIMEOUT);
-            break;
-          }
-          const int q0 = kt * KK::kChunksPerTile;
-          const int nch = min(KK::kChunksPerTile, nq - q0);
-          const uint32_t sf_bytes = (uint32_t)nch * 512u;
-          const uint32_t tx = A_BYTES + B_BYTES + sf_bytes * (rg1 ? 3u : 2u);
-          const uint32_t st = sbase + (uint32_t)s * STAGE_BYTES;
-          mbar_expect_tx(bar_full + 8 * s, tx);
-          tma_load_2d(st, &tmA, kt * KROW, m0, bar_full + 8 * s);
-          tma_load_2d(st + A_BYTES, &tmB, kt * KROW, n0, bar_full + 8 * s);
-          bulk_load(st + SFA_OFF, p.sfa + ((size_t)(m0 / 128) * nq + q0) * 512, sf_bytes, bar_full + 8 * s);
-          bulk_load(st + SFB_OFF, p.sfb + ((size_t)(n0 / 128) * nq + q0) * 512, sf_bytes, bar_full + 8 * s);
-          if (rg1)
-            bulk_load(st + SFB_OFF + KK::kChunksPerTile * 512, p.sfb + ((size_t)(n0 / 128 + 1) * nq + q0) * 512,
-                      sf_bytes, bar_full + 8 * s);
-        }
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
-      uint32_t it = 0, tl = 0;
-      for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tl) {
-        if (!mbar_wait(bar_acc_empty, (tl & 1u) ^ 1u, abort_flag)) {
-          *abort_flag = 1;
-          raise_status(p.status, FP4Q_DEV_TIMEOUT);
-          break;
-        }
-        tc_fence_after();
-        bool ok = true;
-        for (int kt = 0; kt < num_kt; ++kt, ++it) {
-          const int s = (int)(it % STAGES);
-          const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(bar_full + 8 * s, ph, abort_flag)) {
-            *abort_flag = 1;
-            raise_status(p.status, FP4Q_DEV_TIMEOUT);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t st = sbase + (uint32_t)s * STAGE_BYTES;
-          const uint32_t sfa_col = tmem + SF_COL0 + SF_COLS_PER_STAGE * (uint32_t)s;
-          const uint32_t sfb_col = sfa_col + 16;
-          const int q0 = kt * KK::kChunksPerTile;
-          const int nch = min(KK::kChunksPerTile, nq - q0);
-          for (int c = 0; c < nch; ++c) {
-            tc_cp_sf(sfa_col + 4 * c, sf_desc(st + SFA_OFF + 512 * c));
-            tc_cp_sf(sfb_col + 8 * c, sf_desc(st + SFB_OFF + 512 * c));
-            tc_cp_sf(sfb_col + 8 * c + 4, sf_desc(st + SFB_OFF + KK::kChunksPerTile * 512 + 512 * c));
-          }
-          const int rem = p.K - kt * KK::kElemsPerTile;
-          const int n_mma = min(4, rem / KK::kMmaK);
-          for (int k = 0; k < n_mma; ++k) {
-            uint32_t sfa = sfa_col, sfb = sfb_col, sf_id = 0;
-            if constexpr (KIND == KIND_MXF4) {
-              sfa += 4 * (k >> 1);
-              sfb += 8 * (k >> 1);
-              sf_id = 2u * (uint32_t)(k & 1);
-            } else if constexpr (KIND == KIND_NVF4) {
-              sfa += 4 * k;
-              sfb += 8 * k;
-            } else {
-              sf_id = (uint32_t)k;
-            }
-            tc_mma<KIND>(tmem + ACC_COL, op_desc(st + 32 * k), op_desc(st + A_BYTES + 32 * k),
-                         make_idesc<KIND>(sf_id), sfa, sfb, (kt > 0 || k > 0) ? 1u : 0u);
-          }
-          tc_commit(bar_empty + 8 * s);
-        }
-        if (!ok) break;
-        tc_commit(bar_acc_full);
-      }
-    }
-    __syncwarp();
-  } else {
-    // ---------------- epilogue (warps 2..5 -> TMEM lane quarters 2, 3, 0, 1)
-    const int sp = warp & 3;
-    const uint32_t lane_base = tmem + ((uint32_t)(32 * sp) << 16) + ACC_COL;
-    float alpha = 1.0f;
-    if constexpr (KIND == KIND_NVF4) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
-    uint32_t tl = 0;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++tl) {
-      const int m0 = (tile / n_blocks) * BM, n0 = (tile % n_blocks) * BN;
-      const int row = m0 + 32 * sp + lane;
-      bool ok = mbar_wait(bar_acc_full, tl & 1u, abort_flag);
-      ok = __all_sync(0xFFFFFFFFu, ok);
-      if (!ok) {
-        if (lane == 0) {
-          *abort_flag = 1;
-          raise_status(p.status, FP4Q_DEV_TIMEOUT);
-        }
-        break;
-      }
-      tc_fence_after();
-      const int ncols = min(BN, p.N - n0);   // a multiple of 128
-      if (p.d_f32 == nullptr) {
-        // bf16 only: whole row to registers, release TMEM, then store
-        uint32_t h[BN / 2];
-#pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          if (c0 < ncols) {
-            uint32_t r[32];
-            tmem_ld32(lane_base + (uint32_t)c0, r);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              float a = __uint_as_float(r[2 * j]), b = __uint_as_float(r[2 * j + 1]);
-              if constexpr (KIND == KIND_NVF4) {
-                a = __fmul_rn(a, alpha);
-                b = __fmul_rn(b, alpha);
-              }
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(a, b);
-              h[c0 / 2 + j] = *reinterpret_cast<const uint32_t*>(&b2);
-            }
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_acc_empty) : "memory");
-        uint4* dst = reinterpret_cast<uint4*>(p.d_bf16 + (size_t)row * p.N + n0);
-#pragma unroll
-        for (int j = 0; j < BN / 8; ++j)
-          if (8 * j < ncols) dst[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-      } else {
-        // fp32 (and optional bf16): chunk by chunk, TMEM released at the end
-        for (int c0 = 0; c0 < ncols; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(lane_base + (uint32_t)c0, r);
-          float v[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            v[j] = __uint_as_float(r[j]);
-            if constexpr (KIND == KIND_NVF4) v[j] = __fmul_rn(v[j], alpha);
-          }
-          const size_t off = (size_t)row * p.N + n0 + c0;
-          float4* df = reinterpret_cast<float4*>(p.d_f32 + off);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) df[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          if (p.d_bf16) {
-            uint32_t hb[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-              hb[j] = *reinterpret_cast<const uint32_t*>(&b2);
-            }
-            uint4* db = reinterpret_cast<uint4*>(p.d_bf16 + off);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) db[j] = make_uint4(hb[4 * j], hb[4 * j + 1], hb[4 * j + 2], hb[4 * j + 3]);
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_acc_empty) : "memory");
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
-  }
-}
-
-
-// ------------------------------------------------------------ CTA-pair kernel
-// Two CTAs of a cluster share one 256 x 256 output tile through
-// tcgen05.mma.cta_group::2 (M = 256 across the pair, N = 256): each CTA loads
-// its own 128 rows of A and its own 128-row half of B (so each SM moves 32 KB
-// of operands per K-tile instead of 48 KB), plus the scale chunks of its A rows
-// and of both B row groups, and signals the leader CTA's full barrier
-// (cp.async.bulk.tensor ... .cta_group::2).  The leader (cluster rank 0)
-// copies scales to TMEM and issues the MMAs for both; commits are multicast to
-// both CTAs' empty / accumulator barriers; each CTA's epilogue drains its own
-// 128 accumulator rows and releases them with an arrive on the leader.
-namespace pairk {
-
-constexpr int A_BYTES = 128 * KROW;   // this CTA's 128 rows of A
-constexpr int B_BYTES = 128 * KROW;   // this CTA's half of B
-
-template <int KIND>
-struct Layout {
-  static constexpr int kSfChunk = KindK<KIND>::kChunksPerTile * 512;   // one row group, one K-tile
-  static constexpr int SFA_OFF = A_BYTES + B_BYTES;
-  static constexpr int SFB_OFF = SFA_OFF + kSfChunk;
-  static constexpr int STAGE = ((SFB_OFF + 2 * kSfChunk) + 1023) / 1024 * 1024;
-  static constexpr int STAGES = KIND == KIND_NVF4 ? 5 : 6;
-  static constexpr int BAR_OFF = STAGES * STAGE;
-  static constexpr int SMEM = BAR_OFF + 256 + 1024;
-  static constexpr uint32_t SF_COLS = 12u * KindK<KIND>::kChunksPerTile;   // SFA 4/chunk + SFB 8/chunk
-  static constexpr uint32_t TX = A_BYTES + B_BYTES + 3 * kSfChunk;        // bytes one CTA lands per stage
-  static_assert(BAR_OFF + 256 + 1024 <= 232448, "shared memory");
-  static_assert(256 + STAGES * SF_COLS <= TMEM_COLS, "tensor memory");
-};
-
+// ------------------------------------------------------------ cluster helpers
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
+// shared::cluster address of `saddr` in the CTA of cluster rank `rank`
 __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
   uint32_t d;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
@@ -478,6 +277,7 @@ __device__ __forceinline__ void remote_expect_tx(uint32_t cluster_bar, uint32_t 
 __device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
+// TMA load into this CTA's shared memory that signals the pair leader's mbarrier.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* tm, int32_t x, int32_t y,
                                                  uint32_t cluster_bar) {
   asm volatile(
@@ -486,18 +286,17 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       "l"(tm), "r"(x), "r"(y), "r"(cluster_bar)
       : "memory");
 }
-__device__ __forceinline__ void tc_cp_sf2(uint32_t taddr, uint64_t desc) {
-  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
-}
-__device__ __forceinline__ void tc_commit2(uint32_t bar) {
+// Commit of the pair's tensor-core work, arriving on the barrier at this
+// offset in both CTAs.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
       "h"((uint16_t)3)
       : "memory");
 }
 template <int KIND>
-__device__ __forceinline__ void tc_mma2(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
-                                        uint32_t sfb, uint32_t acc) {
+__device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                            uint32_t sfb, uint32_t acc) {
   if constexpr (KIND == KIND_MXF4) {
     asm volatile(
         "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n\t"
@@ -519,116 +318,145 @@ __device__ __forceinline__ void tc_mma2(uint32_t d, uint64_t a, uint64_t b, uint
   }
 }
 
-template <int KIND>
+// ------------------------------------------------------------ the kernel
+// Persistent.  Single CTA (PAIR = false): CTA b owns the 128 x 256 tiles b,
+// b + G, b + 2G, ... (G = gridDim.x).  CTA pair (PAIR = true, clusters of
+// two): pair c owns the 256 x 256 tiles c, c + G/2, ...; cluster rank r holds
+// accumulator rows 128r..128r+127 of each, loads those rows of A and rows
+// 128r..128r+127 of the tile's B, and tcgen05.mma.cta_group::2 issued by rank
+// 0 (the leader) reads both CTAs' operands, so each SM moves 32 KB of A/B per
+// K-tile instead of 48 KB and its tensor core reads half of B from the peer.
+// Tile id -> (m block = id / n_blocks, n block = id % n_blocks).
+template <int KIND, bool PAIR, int QG = -1, int QR = FP4Q_RTNE>
 __global__ void __launch_bounds__(NTHREADS, 1)
-    bs_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
-                        const GemmParams p) {
-  using KK = KindK<KIND>;
-  using L = Layout<KIND>;
+    bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmDh, const __grid_constant__ CUtensorMap tmDf,
+                   const GemmParams p) {
+  using KK = KindK<KIND, PAIR>;
+  constexpr int S = KK::kStages;
+  constexpr int TM = PAIR ? 256 : BM;                         // tile rows
+  constexpr int SFA_OFF = A_BYTES + KK::kBBytes;              // compact chunks: A, B group 0, B group 1
+  constexpr uint32_t SF_COLS = KK::kSfColsA + KK::kSfColsB;   // per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar_full = sbase + L::BAR_OFF;
-  const uint32_t bar_empty = bar_full + 8 * L::STAGES;
-  const uint32_t bar_acc_full = bar_empty + 8 * L::STAGES;
+  const uint32_t stg_base = sbase + S * KK::kStage;
+  const uint32_t bar_full = sbase + KK::kBarOff;       // S: A/B of the stage landed (leader: both CTAs')
+  const uint32_t bar_empty = bar_full + 8 * S;         // S: the stage's MMAs finished
+  const uint32_t bar_sfd = bar_empty + 8 * S;          // S: this CTA's compact scale chunks landed
+  const uint32_t bar_sf = bar_sfd + 8 * S;             // S: scales in TMEM (leader: both CTAs')
+  const uint32_t bar_acc_full = bar_sf + 8 * S;
   const uint32_t bar_acc_empty = bar_acc_full + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::BAR_OFF + 16 * L::STAGES + 16);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::BAR_OFF + 16 * L::STAGES + 24);
+  const uint32_t bar_drain = bar_acc_empty + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + KK::kBarOff + 32 * S + 24);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + KK::kBarOff + 32 * S + 32);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_rank();
+  const uint32_t rank = PAIR ? cluster_rank() : 0u;
   const bool leader = rank == 0;
-  const int n_blocks = (p.N + 255) / 256;
-  const int n_tiles = ((p.M + 255) / 256) * n_blocks;
+  const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;    // pair or CTA index
+  const int n_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int n_blocks = (p.N + BN - 1) / BN;
+  const int n_tiles = ((p.M + TM - 1) / TM) * n_blocks;
   const int num_kt = (p.K + KK::kElemsPerTile - 1) / KK::kElemsPerTile;
-  const int nq = p.K / KK::kBlock / 4;
-  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int nq = p.K / KK::kBlock / 4;   // scale chunks per 128-row group
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < L::STAGES; ++s) {
-      mbar_init(bar_full + 8 * s, 2);    // one expect_tx arrival from each CTA's producer
-      mbar_init(bar_empty + 8 * s, 1);   // the leader's multicast commit
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_full + 8 * s, PAIR ? 2 : 1);   // one expect_tx arrival per producer
+      mbar_init(bar_empty + 8 * s, 1);             // the (leader's) commit
+      mbar_init(bar_sfd + 8 * s, 1);
+      mbar_init(bar_sf + 8 * s, PAIR ? 8 : 4);     // one arrival per scale-writer warp
     }
     mbar_init(bar_acc_full, 1);
-    mbar_init(bar_acc_empty, 8);         // every epilogue warp of both CTAs
+    mbar_init(bar_acc_empty, PAIR ? 8 : 4);        // one arrival per epilogue warp
+    mbar_init(bar_drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    if constexpr (PAIR) {
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                   "r"(TMEM_COLS)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
-  cluster_sync();
+  if constexpr (PAIR) cluster_sync();
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t lead_full = mapa(bar_full, 0);
-  const uint32_t lead_acc_empty = mapa(bar_acc_empty, 0);
+  // barriers the leader owns, as seen from this CTA
+  const uint32_t lead_full = PAIR ? mapa(bar_full, 0) : bar_full;
+  const uint32_t lead_sf = PAIR ? mapa(bar_sf, 0) : bar_sf;
+  const uint32_t lead_acc_empty = PAIR ? mapa(bar_acc_empty, 0) : bar_acc_empty;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- producer (both CTAs)
+      // ---------------- producer
       asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
       uint32_t it = 0;
-      for (int tile = pair; tile < n_tiles && !*abort_flag; tile += npairs) {
-        const int m0 = (tile / n_blocks) * 256, n0 = (tile % n_blocks) * 256;
+      for (int tile = unit; tile < n_tiles && !*abort_flag; tile += n_units) {
+        const int m0 = (tile / n_blocks) * TM + BM * (int)rank, n0 = (tile % n_blocks) * BN;
+        const bool rg1 = (n0 + 128) < p.N;   // the tile's second 128-row group of B exists
+        const bool rows = m0 < p.M;          // this CTA's rows of A exist (false only for a 128-row tail)
         for (int kt = 0; kt < num_kt; ++kt, ++it) {
-          const int s = (int)(it % L::STAGES);
-          const uint32_t ph = (it / L::STAGES) & 1u;
+          const int s = (int)(it % S);
+          const uint32_t ph = (it / S) & 1u;
           if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag)) {
             *abort_flag = 1;
             raise_status(p.status, FP4Q_DEV_TIMEOUT);
             break;
           }
-          const uint32_t st = sbase + (uint32_t)s * L::STAGE;
-          const uint32_t fb = lead_full + 8 * s;
-          const int q0 = kt * KK::kChunksPerTile;
-          remote_expect_tx(fb, L::TX);
-          tma_load_2d_pair(st, &tmA, kt * KROW, m0 + 128 * (int)rank, fb);
-          tma_load_2d_pair(st + A_BYTES, &tmB, kt * KROW, n0 + 128 * (int)rank, fb);
-          tma_load_2d_pair(st + L::SFA_OFF, &tmSA, 0, (m0 / 128 + (int)rank) * nq + q0, fb);
-          tma_load_2d_pair(st + L::SFB_OFF, &tmSB, 0, (n0 / 128) * nq + q0, fb);
-          tma_load_2d_pair(st + L::SFB_OFF + L::kSfChunk, &tmSB, 0, (n0 / 128 + 1) * nq + q0, fb);
+          const int q0 = kt * KK::kChunks;
+          const int nch = min(KK::kChunks, nq - q0);
+          const uint32_t sf_bytes = (uint32_t)nch * 512u;
+          const uint32_t st = sbase + (uint32_t)s * KK::kStage;
+          const uint32_t fb = lead_full + 8 * s, sb = bar_sfd + 8 * s;
+          if constexpr (PAIR) {
+            remote_expect_tx(fb, A_BYTES + KK::kBBytes);
+            tma_load_2d_pair(st, &tmA, kt * KROW, m0, fb);
+            tma_load_2d_pair(st + A_BYTES, &tmB, kt * KROW, n0 + 128 * (int)rank, fb);
+          } else {
+            mbar_expect_tx(fb, A_BYTES + KK::kBBytes);
+            tma_load_2d(st, &tmA, kt * KROW, m0, fb);
+            tma_load_2d(st + A_BYTES, &tmB, kt * KROW, n0, fb);
+          }
+          mbar_expect_tx(sb, sf_bytes * ((rows ? 1u : 0u) + (rg1 ? 2u : 1u)));
+          if (rows) bulk_load(st + SFA_OFF, p.sfa + ((size_t)(m0 / 128) * nq + q0) * 512, sf_bytes, sb);
+          bulk_load(st + SFA_OFF + KK::kChunks * 512, p.sfb + ((size_t)(n0 / 128) * nq + q0) * 512, sf_bytes, sb);
+          if (rg1)
+            bulk_load(st + SFA_OFF + 2 * KK::kChunks * 512, p.sfb + ((size_t)(n0 / 128 + 1) * nq + q0) * 512,
+                      sf_bytes, sb);
         }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
+    // ---------------- MMA issue (lane 0 of the leader)
     if (lane == 0 && leader) {
-      // ---------------- MMA issuer (leader only)
       uint32_t it = 0, tl = 0;
-      for (int tile = pair; tile < n_tiles; tile += npairs, ++tl) {
-        if (!mbar_wait(bar_acc_empty, (tl & 1u) ^ 1u, abort_flag)) {
-          *abort_flag = 1;
-          raise_status(p.status, FP4Q_DEV_TIMEOUT);
-          break;
-        }
+      bool ok = true;
+      for (int tile = unit; tile < n_tiles && ok; tile += n_units, ++tl) {
+        ok = mbar_wait(bar_acc_empty, (tl & 1u) ^ 1u, abort_flag);
+        if (!ok) break;
         tc_fence_after();
-        bool ok = true;
         for (int kt = 0; kt < num_kt; ++kt, ++it) {
-          const int s = (int)(it % L::STAGES);
-          const uint32_t ph = (it / L::STAGES) & 1u;
-          if (!mbar_wait(bar_full + 8 * s, ph, abort_flag)) {
-            *abort_flag = 1;
-            raise_status(p.status, FP4Q_DEV_TIMEOUT);
-            ok = false;
-            break;
-          }
+          const int s = (int)(it % S);
+          const uint32_t ph = (it / S) & 1u;
+          ok = mbar_wait(bar_full + 8 * s, ph, abort_flag) && mbar_wait(bar_sf + 8 * s, ph, abort_flag);
+          if (!ok) break;
           tc_fence_after();
-          const uint32_t st = sbase + (uint32_t)s * L::STAGE;
-          const uint32_t sfa_col = tmem + 256 + L::SF_COLS * (uint32_t)s;
-          const uint32_t sfb_col = sfa_col + 4 * KK::kChunksPerTile;
-          const int q0 = kt * KK::kChunksPerTile;
-          const int nch = min(KK::kChunksPerTile, nq - q0);
-          for (int c = 0; c < nch; ++c) {
-            tc_cp_sf2(sfa_col + 4 * c, sf_desc(st + L::SFA_OFF + 512 * c));
-            tc_cp_sf2(sfb_col + 8 * c, sf_desc(st + L::SFB_OFF + 512 * c));
-            tc_cp_sf2(sfb_col + 8 * c + 4, sf_desc(st + L::SFB_OFF + L::kSfChunk + 512 * c));
-          }
+          const uint32_t st = sbase + (uint32_t)s * KK::kStage;
+          const uint32_t sfa_col = tmem + ACC_COL + BN + SF_COLS * (uint32_t)s;
+          const uint32_t sfb_col = sfa_col + KK::kSfColsA;
           const int rem = p.K - kt * KK::kElemsPerTile;
           const int n_mma = min(4, rem / KK::kMmaK);
           for (int k = 0; k < n_mma; ++k) {
@@ -643,26 +471,91 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             } else {
               sf_id = (uint32_t)k;
             }
-            tc_mma2<KIND>(tmem + ACC_COL, op_desc(st + 32 * k), op_desc(st + A_BYTES + 32 * k),
-                          make_idesc<KIND, 256>(sf_id), sfa, sfb, (kt > 0 || k > 0) ? 1u : 0u);
+            const uint32_t acc = (kt > 0 || k > 0) ? 1u : 0u;
+            if constexpr (PAIR)
+              tc_mma_pair<KIND>(tmem + ACC_COL, op_desc(st + 32 * k), op_desc(st + A_BYTES + 32 * k),
+                                make_idesc<KIND, TM>(sf_id), sfa, sfb, acc);
+            else
+              tc_mma<KIND>(tmem + ACC_COL, op_desc(st + 32 * k), op_desc(st + A_BYTES + 32 * k),
+                           make_idesc<KIND, TM>(sf_id), sfa, sfb, acc);
           }
-          tc_commit2(bar_empty + 8 * s);
+          if constexpr (PAIR) tc_commit_pair(bar_empty + 8 * s);
+          else tc_commit(bar_empty + 8 * s);
         }
         if (!ok) break;
-        tc_commit2(bar_acc_full);
+        if constexpr (PAIR) tc_commit_pair(bar_acc_full);
+        else tc_commit(bar_acc_full);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        raise_status(p.status, FP4Q_DEV_TIMEOUT);
+      }
+      // wait (bounded) until every tensor-core operation this lane issued finished
+      if constexpr (PAIR)
+        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar_drain)
+                     : "memory");
+      else
+        tc_commit(bar_drain);
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try(bar_drain, 0) && globaltimer() - t0 < 2000000000ull) {
       }
     }
     __syncwarp();
+  } else if (warp >= 6) {
+    // ---------------- scale writers: lane i of quarter q stores row i of the compact chunks
+    const uint32_t qbase = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int tile = unit; tile < n_tiles && ok; tile += n_units) {
+      for (int kt = 0; kt < num_kt; ++kt, ++it) {
+        const int s = (int)(it % S);
+        const uint32_t ph = (it / S) & 1u;
+        ok = mbar_wait(bar_sfd + 8 * s, ph, abort_flag);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t st = sbase + (uint32_t)s * KK::kStage;
+        const uint32_t ca = st + SFA_OFF, cb0 = ca + KK::kChunks * 512, cb1 = cb0 + KK::kChunks * 512;
+        const uint32_t sfa_col = qbase + ACC_COL + BN + SF_COLS * (uint32_t)s;
+        const uint32_t sfb_col = sfa_col + KK::kSfColsA;
+        if constexpr (KIND == KIND_F8) {
+          tmem_st4(sfa_col, chunk_row(ca, lane));
+        } else {
+#pragma unroll
+          for (int pr = 0; pr < KK::kChunks / 2; ++pr)
+            tmem_st8(sfa_col + 8 * pr, chunk_row(ca + 1024u * pr, lane), chunk_row(ca + 1024u * pr + 512u, lane));
+        }
+#pragma unroll
+        for (int c = 0; c < KK::kChunks; ++c)
+          tmem_st8(sfb_col + 8 * c, chunk_row(cb0 + 512u * c, lane), chunk_row(cb1 + 512u * c, lane));
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (PAIR) remote_arrive(lead_sf + 8 * s);
+          else mbar_arrive(lead_sf + 8 * s);
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      raise_status(p.status, FP4Q_DEV_TIMEOUT);
+    }
   } else {
-    // ---------------- epilogue (both CTAs; warps 2..5 -> TMEM lane quarters 2, 3, 0, 1)
+    // ---------------- epilogue (warps 2..5 -> TMEM lane quarters 2, 3, 0, 1)
     const int sp = warp & 3;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * sp) << 16) + ACC_COL;
+    const uint32_t stg = stg_base + (uint32_t)(warp - 2) * STG_BYTES;   // one store box per warp
+    // 128B-swizzled box row `lane`: 16-byte unit u of the row sits at unit u ^ (lane & 7)
+    const uint32_t row_off = 128u * (uint32_t)lane;
+    const uint32_t swz = (uint32_t)(lane & 7);
     float alpha = 1.0f;
     if constexpr (KIND == KIND_NVF4) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
     uint32_t tl = 0;
-    for (int tile = pair; tile < n_tiles; tile += npairs, ++tl) {
-      const int m0 = (tile / n_blocks) * 256 + 128 * (int)rank, n0 = (tile % n_blocks) * 256;
-      const int row = m0 + 32 * sp + lane;
+    for (int tile = unit; tile < n_tiles; tile += n_units, ++tl) {
+      const int m0 = (tile / n_blocks) * TM + BM * (int)rank, n0 = (tile % n_blocks) * BN;
+      const int y = m0 + 32 * sp;
+      const bool live = m0 < p.M;   // false only for the second CTA of a 128-row tail tile
       bool ok = mbar_wait(bar_acc_full, tl & 1u, abort_flag);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) {
@@ -673,80 +566,107 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         break;
       }
       tc_fence_after();
-      const int ncols = min(BN, p.N - n0);
-      const bool live = m0 < p.M;   // the follower's rows of a 128-row tail tile lie outside the matrix
-      if (p.d_f32 == nullptr) {
-        uint32_t h[BN / 2];
+      const int ncols = min(BN, p.N - n0);   // 128 or 256
+      uint32_t h[BN / 2];                    // the row as packed bf16
 #pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          if (c0 < ncols) {
-            uint32_t r[32];
-            tmem_ld32(lane_base + (uint32_t)c0, r);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              float a = __uint_as_float(r[2 * j]), b = __uint_as_float(r[2 * j + 1]);
-              if constexpr (KIND == KIND_NVF4) {
-                a = __fmul_rn(a, alpha);
-                b = __fmul_rn(b, alpha);
-              }
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(a, b);
-              h[c0 / 2 + j] = *reinterpret_cast<const uint32_t*>(&b2);
-            }
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) remote_arrive(lead_acc_empty);
-        if (live) {
-          uint4* dst = reinterpret_cast<uint4*>(p.d_bf16 + (size_t)row * p.N + n0);
-#pragma unroll
-          for (int j = 0; j < BN / 8; ++j)
-            if (8 * j < ncols) dst[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-        }
-      } else {
-        for (int c0 = 0; c0 < ncols; c0 += 32) {
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        if (c0 < ncols) {
           uint32_t r[32];
           tmem_ld32(lane_base + (uint32_t)c0, r);
-          if (!live) continue;
-          float v[32];
+          if constexpr (KIND == KIND_NVF4) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            v[j] = __uint_as_float(r[j]);
-            if constexpr (KIND == KIND_NVF4) v[j] = __fmul_rn(v[j], alpha);
+            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), alpha));
           }
-          const size_t off = (size_t)row * p.N + n0 + c0;
-          float4* df = reinterpret_cast<float4*>(p.d_f32 + off);
+          if (p.want_f32 && live) {
+            // one 32-row x 32-float box per 32 columns
+            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 8; ++j) df[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          if (p.d_bf16) {
-            uint32_t hb[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-              hb[j] = *reinterpret_cast<const uint32_t*>(&b2);
+            for (int u = 0; u < 8; ++u)
+              st_shared16(stg + row_off + 16u * ((uint32_t)u ^ swz),
+                          make_uint4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]));
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmDf, n0 + c0, y, stg);
+              asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             }
-            uint4* db = reinterpret_cast<uint4*>(p.d_bf16 + off);
+          }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) db[j] = make_uint4(hb[4 * j], hb[4 * j + 1], hb[4 * j + 2], hb[4 * j + 3]);
+          for (int j = 0; j < 16; ++j) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+            h[c0 / 2 + j] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          if constexpr (QG >= 0) {
+            // quantize this row's 32 bf16 outputs as the next operand's row-wise chunk
+            if (live) {
+              uint32_t w[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) w[j] = h[c0 / 2 + j];
+              float2 P[16];
+              chunk_from_bf16_words(w, p.q_sgn, P);
+              if (p.q_nh == 16) rotate_chunk<16>(P);
+              else if (p.q_nh == 32) rotate_chunk<32>(P);
+              ChunkOut o;
+              const int64_t row = (int64_t)y + lane, col = (int64_t)n0 + c0;
+              quantize_chunk<QG, FP4Q_SCALE_MX, QR>(P, 0.0f, (uint64_t)(row * p.N + col), 0u, (uint32_t)p.q_seed,
+                                                    (uint32_t)(p.q_seed >> 32), p.q_e4m3 != nullptr, p.status, o);
+              *reinterpret_cast<uint4*>(p.q_codes + row * (p.N / 2) + col / 2) = make_uint4(o.w[0], o.w[1], o.w[2], o.w[3]);
+              const int64_t nkb = p.N / 32, k = col / 32;
+              p.q_scales[p.q_sf_mma ? sf_mma_offset(row, k, nkb) : row * nkb + k] = (uint8_t)o.sbytes;
+              if (p.q_e4m3) {
+                uint4* ep = reinterpret_cast<uint4*>(p.q_e4m3 + row * p.N + col);
+                ep[0] = make_uint4(o.e4[0], o.e4[1], o.e4[2], o.e4[3]);
+                ep[1] = make_uint4(o.e4[4], o.e4[5], o.e4[6], o.e4[7]);
+              }
+            }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) remote_arrive(lead_acc_empty);
+      }
+      // accumulator consumed: let the next tile's MMAs start
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (PAIR) remote_arrive(lead_acc_empty);
+        else mbar_arrive(lead_acc_empty);
+      }
+      if (p.want_bf16 && live) {
+        // one 32-row x 64-bf16 box per 64 columns
+#pragma unroll
+        for (int b = 0; b < BN / 64; ++b) {
+          if (64 * b < ncols) {
+            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              st_shared16(stg + row_off + 16u * ((uint32_t)u ^ swz),
+                          make_uint4(h[32 * b + 4 * u], h[32 * b + 4 * u + 1], h[32 * b + 4 * u + 2],
+                                     h[32 * b + 4 * u + 3]));
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmDh, n0 + 64 * b, y, stg);
+              asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            }
+          }
+        }
       }
     }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
   }
-  // No CTA may leave while its peer can still read its shared memory or
-  // tensor memory: meet, then free the pair's allocation together.
   tc_fence_before();
-  cluster_sync();
+  // no CTA of a pair may leave while its peer can still use its shared or tensor memory
+  if constexpr (PAIR) cluster_sync();
+  else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    if constexpr (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
   }
 }
-
-}  // namespace pairk
 
 // ------------------------------------------------------------ host side
 // 2-D byte tensor [rows][row_bytes], box = 128 bytes x box_rows, 128B swizzle.
@@ -754,64 +674,106 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t row
   return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, (uint32_t)KROW,
                         box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
-
-// Scale factors in the MMA layout viewed as a 2-D u32 tensor: one row per
-// 512-byte chunk (rows / 128 * blocks / 4 chunks), box = chunks of one K-tile.
-bool make_sf_map(CUtensorMap* m, const void* base, uint64_t n_chunks, uint32_t box_chunks) {
-  return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, base, 128u, n_chunks, 512u, 128u, box_chunks,
-                        CU_TENSOR_MAP_SWIZZLE_NONE);
+// Output [M][N] of bf16 (box 64 x 32) or fp32 (box 32 x 32), 128B swizzle.
+bool make_out_map(CUtensorMap* m, const void* base, uint64_t N, uint64_t M, bool f32) {
+  return encode_tmap_2d(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, N, M,
+                        N * (f32 ? 4u : 2u), f32 ? 32u : 64u, 32u, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int KIND>
-cudaError_t launch_gemm_pair(const fp4q_operand* A, const fp4q_operand* B, const void* a_data, const void* b_data,
-                             uint64_t row_bytes, const GemmParams& p, cudaStream_t s) {
-  using L = pairk::Layout<KIND>;
-  CUtensorMap ta, tb, tsa, tsb;
-  const uint64_t nq = (uint64_t)p.K / KindK<KIND>::kBlock / 4;
-  if (!make_map(&ta, a_data, row_bytes, (uint64_t)p.M, 128) || !make_map(&tb, b_data, row_bytes, (uint64_t)p.N, 128) ||
-      !make_sf_map(&tsa, A->scales, (uint64_t)p.M / 128 * nq, KindK<KIND>::kChunksPerTile) ||
-      !make_sf_map(&tsb, B->scales, (uint64_t)p.N / 128 * nq, KindK<KIND>::kChunksPerTile))
-    return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(pairk::bs_gemm_pair_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::SMEM);
+template <int KIND, bool PAIR, int QG = -1, int QR = FP4Q_RTNE>
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& dh, const CUtensorMap& df,
+                        const GemmParams& p, cudaStream_t s) {
+  using KK = KindK<KIND, PAIR>;
+  static unsigned attr_set = 0;   // one bit per device ordinal < 32
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned bit = dev < 32 ? (1u << dev) : 0u;
+  if (!(attr_set & bit) || !bit) {
+    e = cudaFuncSetAttribute(bs_gemm_kernel<KIND, PAIR, QG, QR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             KK::kSmem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set |= bit;
   }
-  const int tiles = ((p.M + 255) / 256) * ((p.N + 255) / 256);
-  int pairs = num_sms() / 2;
-  if (tiles < pairs) pairs = tiles;
+  const int tm = PAIR ? 256 : BM;
+  const int tiles = ((p.M + tm - 1) / tm) * ((p.N + BN - 1) / BN);
+  int units = PAIR ? num_sms() / 2 : num_sms();
+  if (tiles < units) units = tiles;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+  cfg.gridDim = dim3((unsigned)(PAIR ? 2 * units : units), 1, 1);
   cfg.blockDim = dim3(NTHREADS, 1, 1);
-  cfg.dynamicSmemBytes = L::SMEM;
+  cfg.dynamicSmemBytes = KK::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, pairk::bs_gemm_pair_kernel<KIND>, ta, tb, tsa, tsb, p);
-}
-
-template <int KIND>
-cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(bs_gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  const int tiles = (p.M / BM) * ((p.N + BN - 1) / BN);
-  const int g = tiles < num_sms() ? tiles : num_sms();
-  bs_gemm_kernel<KIND><<<g, NTHREADS, SMEM_BYTES, s>>>(a, b, p);
-  return cudaGetLastError();
+  cfg.numAttrs = PAIR ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, bs_gemm_kernel<KIND, PAIR, QG, QR>, a, b, dh, df, p);
 }
 
 bool al(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// The single-CTA form is the default: on the linear-layer shapes the pair form
+// measured no faster (both issue one MMA per ~190 cycles per SM, limited by
+// shared-memory traffic while TMA refills the ring) and it adds cluster-scope
+// synchronisation.  Building with -DFP4Q_GEMM_PAIR=1 selects the pair form.
+#ifndef FP4Q_GEMM_PAIR
+#define FP4Q_GEMM_PAIR 0
+#endif
+constexpr bool kPair = FP4Q_GEMM_PAIR != 0;
+
+// Checks shared by the two entry points, the kernel parameters and the
+// operand / output tensor maps.  Returns FP4Q_OK or the error status.
+int32_t prepare_gemm(const fp4q_operand* A, const fp4q_operand* B, int64_t M, int64_t N, int64_t K, int32_t grid,
+                     int32_t scale, void* D_bf16, float* D_f32, uint32_t* d_status, int& kind, GemmParams& p,
+                     CUtensorMap& ta, CUtensorMap& tb, CUtensorMap& tdh, CUtensorMap& tdf) {
+  if (!A || !B) return FP4Q_ERR_INVALID_ARG;
+  if (grid != FP4Q_GRID_E2M1 && grid != FP4Q_GRID_E1M2 && grid != FP4Q_GRID_E2M1_R4) return FP4Q_ERR_INVALID_ARG;
+  if (scale != FP4Q_SCALE_MX && scale != FP4Q_SCALE_NV) return FP4Q_ERR_INVALID_ARG;
+  if (grid == FP4Q_GRID_E1M2 && scale == FP4Q_SCALE_NV) return FP4Q_ERR_UNSUPPORTED;
+  if (M <= 0 || N <= 0 || K <= 0) return FP4Q_ERR_INVALID_ARG;
+  if (M % 128 || N % 128) return FP4Q_ERR_INVALID_ARG;
+  if (K % (scale == FP4Q_SCALE_NV ? 64 : 128)) return FP4Q_ERR_INVALID_ARG;
+  if (M / 128 > 65535 || M > (1LL << 31) || N > (1LL << 31) || K > (1LL << 31)) return FP4Q_ERR_INVALID_ARG;
+  kind = grid == FP4Q_GRID_E1M2 ? KIND_F8 : (scale == FP4Q_SCALE_NV ? KIND_NVF4 : KIND_MXF4);
+  const void* a_data = kind == KIND_F8 ? (const void*)A->e4m3 : (const void*)A->codes;
+  const void* b_data = kind == KIND_F8 ? (const void*)B->e4m3 : (const void*)B->codes;
+  if (!a_data || !b_data || !A->scales || !B->scales) return FP4Q_ERR_INVALID_ARG;
+  if (kind == KIND_NVF4 && (!A->tensor_scale || !B->tensor_scale)) return FP4Q_ERR_INVALID_ARG;
+  if (!al(a_data, 16) || !al(b_data, 16) || !al(A->scales, 16) || !al(B->scales, 16)) return FP4Q_ERR_ALIGNMENT;
+  if ((D_bf16 && !al(D_bf16, 16)) || (D_f32 && !al(D_f32, 16))) return FP4Q_ERR_ALIGNMENT;
+  const uint64_t row_bytes = kind == KIND_F8 ? (uint64_t)K : (uint64_t)K / 2;
+  memset(&p, 0, sizeof p);
+  p.sfa = A->scales;
+  p.sfb = B->scales;
+  p.ts_a = A->tensor_scale;
+  p.ts_b = B->tensor_scale;
+  p.status = d_status;
+  p.M = (int32_t)M;
+  p.N = (int32_t)N;
+  p.K = (int32_t)K;
+  p.want_bf16 = D_bf16 != nullptr;
+  p.want_f32 = D_f32 != nullptr;
+  memset(&tdh, 0, sizeof(tdh));
+  memset(&tdf, 0, sizeof(tdf));
+  if (!make_map(&ta, a_data, row_bytes, (uint64_t)M, BM) ||
+      !make_map(&tb, b_data, row_bytes, (uint64_t)N, KindK<KIND_MXF4, kPair>::kBRows))
+    return FP4Q_ERR_CUDA;
+  if (D_bf16 && !make_out_map(&tdh, D_bf16, (uint64_t)N, (uint64_t)M, false)) return FP4Q_ERR_CUDA;
+  if (D_f32 && !make_out_map(&tdf, D_f32, (uint64_t)N, (uint64_t)M, true)) return FP4Q_ERR_CUDA;
+  return FP4Q_OK;
+}
+
+template <int QG, int QR>
+cudaError_t launch_kind(int kind, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tdh,
+                        const CUtensorMap& tdf, const GemmParams& p, cudaStream_t s) {
+  if (kind == KIND_MXF4) return launch_gemm<KIND_MXF4, kPair && QG < 0, QG, QR>(ta, tb, tdh, tdf, p, s);
+  if (kind == KIND_NVF4) return launch_gemm<KIND_NVF4, kPair && QG < 0, QG, QR>(ta, tb, tdh, tdf, p, s);
+  return launch_gemm<KIND_F8, kPair && QG < 0, QG, QR>(ta, tb, tdh, tdf, p, s);
+}
 
 }  // namespace
 }  // namespace fp4q
@@ -820,46 +782,53 @@ extern "C" int32_t fp4q_gemm(const fp4q_operand* A, const fp4q_operand* B, int64
                              int32_t grid, int32_t scale, void* D_bf16, float* D_f32, uint32_t* d_status,
                              void* stream) {
   using namespace fp4q;
-  if (!A || !B || (!D_bf16 && !D_f32)) return FP4Q_ERR_INVALID_ARG;
-  if (grid != FP4Q_GRID_E2M1 && grid != FP4Q_GRID_E1M2 && grid != FP4Q_GRID_E2M1_R4) return FP4Q_ERR_INVALID_ARG;
-  if (scale != FP4Q_SCALE_MX && scale != FP4Q_SCALE_NV) return FP4Q_ERR_INVALID_ARG;
-  if (grid == FP4Q_GRID_E1M2 && scale == FP4Q_SCALE_NV) return FP4Q_ERR_UNSUPPORTED;
-  if (M <= 0 || N <= 0 || K <= 0) return FP4Q_ERR_INVALID_ARG;
-  if (M % 128 || N % 128) return FP4Q_ERR_INVALID_ARG;
-  if (K % (scale == FP4Q_SCALE_NV ? 64 : 128)) return FP4Q_ERR_INVALID_ARG;
-  if (M / 128 > 65535 || M > (1LL << 31) || N > (1LL << 31) || K > (1LL << 31)) return FP4Q_ERR_INVALID_ARG;
-  const int kind = grid == FP4Q_GRID_E1M2 ? KIND_F8 : (scale == FP4Q_SCALE_NV ? KIND_NVF4 : KIND_MXF4);
-  const void* a_data = kind == KIND_F8 ? (const void*)A->e4m3 : (const void*)A->codes;
-  const void* b_data = kind == KIND_F8 ? (const void*)B->e4m3 : (const void*)B->codes;
-  if (!a_data || !b_data || !A->scales || !B->scales) return FP4Q_ERR_INVALID_ARG;
-  if (kind == KIND_NVF4 && (!A->tensor_scale || !B->tensor_scale)) return FP4Q_ERR_INVALID_ARG;
-  if (!al(a_data, 16) || !al(b_data, 16) || !al(A->scales, 16) || !al(B->scales, 16)) return FP4Q_ERR_ALIGNMENT;
-  if ((D_bf16 && !al(D_bf16, 16)) || (D_f32 && !al(D_f32, 16))) return FP4Q_ERR_ALIGNMENT;
-  const uint64_t row_bytes = kind == KIND_F8 ? (uint64_t)K : (uint64_t)K / 2;
+  if (!D_bf16 && !D_f32) return FP4Q_ERR_INVALID_ARG;
+  int kind = 0;
   GemmParams p;
-  p.sfa = A->scales;
-  p.sfb = B->scales;
-  p.ts_a = A->tensor_scale;
-  p.ts_b = B->tensor_scale;
-  p.d_bf16 = static_cast<uint16_t*>(D_bf16);
-  p.d_f32 = D_f32;
-  p.status = d_status;
-  p.M = (int32_t)M;
-  p.N = (int32_t)N;
-  p.K = (int32_t)K;
+  CUtensorMap ta, tb, tdh, tdf;
+  const int32_t st = prepare_gemm(A, B, M, N, K, grid, scale, D_bf16, D_f32, d_status, kind, p, ta, tb, tdh, tdf);
+  if (st != FP4Q_OK) return st;
+  const cudaError_t e = launch_kind<-1, FP4Q_RTNE>(kind, ta, tb, tdh, tdf, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+}
+
+extern "C" int32_t fp4q_gemm_quantize(const fp4q_operand* A, const fp4q_operand* B, int64_t M, int64_t N, int64_t K,
+                                      int32_t grid, int32_t scale, void* D_bf16, const fp4q_config* out_cfg,
+                                      fp4q_operand* out, uint32_t* d_status, void* stream) {
+  using namespace fp4q;
+  if (!out_cfg || !out || !out->codes || !out->scales) return FP4Q_ERR_INVALID_ARG;
+  const fp4q_config& c = *out_cfg;
+  if (c.grid != FP4Q_GRID_E2M1 && c.grid != FP4Q_GRID_E1M2 && c.grid != FP4Q_GRID_E2M1_R4) return FP4Q_ERR_INVALID_ARG;
+  if (c.rot != FP4Q_ROT_NONE && c.rot != FP4Q_ROT_H16 && c.rot != FP4Q_ROT_H32) return FP4Q_ERR_INVALID_ARG;
+  if (c.round != FP4Q_RTNE && c.round != FP4Q_SR) return FP4Q_ERR_INVALID_ARG;
+  if (c.sf_layout != FP4Q_SF_PLAIN && c.sf_layout != FP4Q_SF_MMA) return FP4Q_ERR_INVALID_ARG;
+  // one pass over D: MX scales only (NV needs the global amax of the whole rotated output first),
+  // and only the row-wise copy (the column-wise blocks would span 32 tiles' rows)
+  if (c.scale != FP4Q_SCALE_MX || !c.want_row || c.want_col) return FP4Q_ERR_UNSUPPORTED;
+  if (c.emit_e4m3 && !out->e4m3) return FP4Q_ERR_INVALID_ARG;
+  if (!al(out->codes, 16) || (c.emit_e4m3 && !al(out->e4m3, 16))) return FP4Q_ERR_ALIGNMENT;
+  int kind = 0;
+  GemmParams p;
+  CUtensorMap ta, tb, tdh, tdf;
+  const int32_t st = prepare_gemm(A, B, M, N, K, grid, scale, D_bf16, nullptr, d_status, kind, p, ta, tb, tdh, tdf);
+  if (st != FP4Q_OK) return st;
+  p.q_codes = out->codes;
+  p.q_scales = out->scales;
+  p.q_e4m3 = c.emit_e4m3 ? out->e4m3 : nullptr;
+  p.q_seed = c.sr_seed;
+  p.q_nh = c.rot;
+  p.q_sf_mma = c.sf_layout == FP4Q_SF_MMA;
+  for (int t = 0; t < 32; ++t) p.q_sgn[t] = (c.rot && ((c.sign_mask_row >> (t % c.rot)) & 1u)) ? 0x80000000u : 0u;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-#if FP4Q_GEMM_PAIR
-  if (kind == KIND_MXF4) e = launch_gemm_pair<KIND_MXF4>(A, B, a_data, b_data, row_bytes, p, s);
-  else if (kind == KIND_NVF4) e = launch_gemm_pair<KIND_NVF4>(A, B, a_data, b_data, row_bytes, p, s);
-  else e = launch_gemm_pair<KIND_F8>(A, B, a_data, b_data, row_bytes, p, s);
-#else
-  CUtensorMap ta, tb;
-  if (!make_map(&ta, a_data, row_bytes, (uint64_t)M, BM) || !make_map(&tb, b_data, row_bytes, (uint64_t)N, BN))
-    return FP4Q_ERR_CUDA;
-  if (kind == KIND_MXF4) e = launch_gemm<KIND_MXF4>(ta, tb, p, s);
-  else if (kind == KIND_NVF4) e = launch_gemm<KIND_NVF4>(ta, tb, p, s);
-  else e = launch_gemm<KIND_F8>(ta, tb, p, s);
-#endif
+  if (c.grid == FP4Q_GRID_E2M1)
+    e = c.round == FP4Q_SR ? launch_kind<FP4Q_GRID_E2M1, FP4Q_SR>(kind, ta, tb, tdh, tdf, p, s)
+                           : launch_kind<FP4Q_GRID_E2M1, FP4Q_RTNE>(kind, ta, tb, tdh, tdf, p, s);
+  else if (c.grid == FP4Q_GRID_E1M2)
+    e = c.round == FP4Q_SR ? launch_kind<FP4Q_GRID_E1M2, FP4Q_SR>(kind, ta, tb, tdh, tdf, p, s)
+                           : launch_kind<FP4Q_GRID_E1M2, FP4Q_RTNE>(kind, ta, tb, tdh, tdf, p, s);
+  else
+    e = c.round == FP4Q_SR ? launch_kind<FP4Q_GRID_E2M1_R4, FP4Q_SR>(kind, ta, tb, tdh, tdf, p, s)
+                           : launch_kind<FP4Q_GRID_E2M1_R4, FP4Q_RTNE>(kind, ta, tb, tdh, tdf, p, s);
   return e == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
 }

@@ -33,6 +33,7 @@
 
 #include "fp4q_dev.cuh"
 #include "fp4q_internal.h"
+#include "quant_core.cuh"
 
 namespace fp4q {
 
@@ -45,229 +46,6 @@ namespace fp4q {
 constexpr int kTR = 32;    // tile rows
 constexpr int kTC = 256;   // tile columns
 constexpr int kNT = 256;   // threads per CTA
-
-template <int GRID>
-struct GridK;
-template <>
-struct GridK<FP4Q_GRID_E2M1> {
-  static constexpr float kQmax = 6.0f;
-  static constexpr int kEmax = 2;
-  static constexpr uint32_t kE4T0 = 0x3C383000u, kE4T1 = 0x4C484440u;  // E4M3 bytes of the 8 levels
-};
-template <>
-struct GridK<FP4Q_GRID_E1M2> {
-  static constexpr float kQmax = 1.75f;
-  static constexpr int kEmax = 0;
-  static constexpr uint32_t kE4T0 = 0x34302800u, kE4T1 = 0x3E3C3A38u;
-};
-// E2M1 capped at 4: E2M1 codes 0..6, block maxima scaled into [2, 4).
-template <>
-struct GridK<FP4Q_GRID_E2M1_R4> {
-  static constexpr float kQmax = 4.0f;
-  static constexpr int kEmax = 1;
-  static constexpr uint32_t kE4T0 = 0x3C383000u, kE4T1 = 0x4C484440u;
-};
-
-// Eight packed E2M1 codes with magnitude 7 (6.0) turned into 6 (4.0): the
-// saturation of the capped grid applied after the hardware conversion.
-__device__ __forceinline__ uint32_t cap_e2m1_codes(uint32_t w) {
-  const uint32_t m = w & 0x77777777u;
-  const uint32_t seven = m & (m >> 1) & (m >> 2) & 0x11111111u;   // bit 0 of each nibble whose low 3 bits are 111
-  return w ^ seven;
-}
-
-// ------------------------------------------------------------ rounding
-// RTNE onto {k/4}: clamp |v| to 1.75, then k = RNE(4|v|) read from the low
-// mantissa bits of 4|v| + 2^23 (exact product, one rounding).
-__device__ __forceinline__ uint32_t rtne_e1m2(float v) {
-  const float a = fminf(fabsf(v), 1.75f);
-  const float t = __fmaf_rn(a, 4.0f, 8388608.0f);
-  return (__float_as_uint(t) & 7u) | ((__float_as_uint(v) >> 28) & 8u);
-}
-
-// Exact stochastic-rounding decision shared by both grids.  With s >= 0 the
-// position on a unit-spaced grid (s < 8), t = fl_rm(s + 2^23) holds floor(s) in
-// its low bits; C = 2^23 - floor(s) 2^16 is exact; y = fl_ru(s 2^16 + C) =
-// 2^23 + ceil(frac(s) 2^16); and r16 < frac(s) 2^16 (the rule r / 2^16 < f)
-// holds iff 2^23 + r16 < y.  Returns floor(s) + up.
-__device__ __forceinline__ uint32_t sr_unit(float s, float r_as_float) {
-  float t, y;
-  asm("add.rm.f32 %0, %1, %2;" : "=f"(t) : "f"(s), "f"(8388608.0f));
-  const float C = __fmaf_rn(t, -65536.0f, 549764202496.0f);   // 2^39 + 2^23 - t 2^16
-  asm("fma.rp.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(s), "f"(65536.0f), "f"(C));
-  return (__float_as_uint(t) & 7u) + ((r_as_float < y) ? 1u : 0u);
-}
-
-// 2^23 + r as a float, r the 16-bit uniform numerator (exact).
-__device__ __forceinline__ float r16_float(uint32_t r16) { return __uint_as_float(0x4B000000u | r16); }
-
-// SR onto {k/4}: s = 4 min(|v|, 1.75) is exact and lies on the unit grid.
-__device__ __forceinline__ uint32_t sr_e1m2(float v, float rf) {
-  const float s = fminf(fabsf(v), 1.75f) * 4.0f;
-  return sr_unit(s, rf) | ((__float_as_uint(v) >> 28) & 8u);
-}
-
-// SR onto E2M1: with E = clamp(floor(log2 |v|), 0, 2) the levels around |v|
-// are 2^(E-1) apart, s = |v| 2^(1-E) is exact, and the lower level's code is
-// 2E + floor(s) (floor(s) = 0..3 for E = 0, 2..3 above).
-template <int CAP = 6>
-__device__ __forceinline__ uint32_t sr_e2m1(float v, float rf) {
-  const float a = fminf(fabsf(v), (float)CAP);
-  const uint32_t eb = __float_as_uint(fmaxf(a, 1.0f)) & 0x7F800000u;   // (127 + E) << 23
-  const float s = a * __uint_as_float(0x7F800000u - eb);              // 2^(1-E), exponent 128 - E
-  const uint32_t twoE = (eb >> 22) - 254u;
-  return (twoE + sr_unit(s, rf)) | ((__float_as_uint(v) >> 28) & 8u);
-}
-
-// E4M3 bytes of eight packed codes (element 0 in the low nibble): magnitude by
-// byte permutation of the level table, sign from bit 3 of each nibble.
-template <int GRID>
-__device__ __forceinline__ uint2 codes_to_e4m3(uint32_t w) {
-  const uint32_t lo = __byte_perm(GridK<GRID>::kE4T0, GridK<GRID>::kE4T1, w & 0x7777u) |
-                      __byte_perm(0u, 0x80808080u, (w >> 1) & 0x4444u);
-  const uint32_t hw = w >> 16;
-  const uint32_t hi = __byte_perm(GridK<GRID>::kE4T0, GridK<GRID>::kE4T1, hw & 0x7777u) |
-                      __byte_perm(0u, 0x80808080u, (hw >> 1) & 0x4444u);
-  return make_uint2(lo, hi);
-}
-
-// ------------------------------------------------------------ one chunk
-// Rotation of a chunk held as P[i] = (u[i], u[i+16]) (signs already applied).
-template <int NH>
-__device__ __forceinline__ void rotate_chunk(float2 (&P)[16]) {
-  if constexpr (NH == 16 || NH == 32) {
-#pragma unroll
-    for (int h = 1; h < 16; h <<= 1) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if (i & h) continue;
-        const float2 a = P[i], b = P[i + h];
-        P[i] = add2(a, b);
-        P[i + h] = sub2(a, b);
-      }
-    }
-    if constexpr (NH == 32) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float a = P[i].x, b = P[i].y;
-        P[i].x = __fadd_rn(a, b);
-        P[i].y = __fsub_rn(a, b);
-      }
-    }
-    const float c = (NH == 16) ? 0.25f : __uint_as_float(0x3E3504F3u);  // fl32(1/sqrt(32))
-#pragma unroll
-    for (int i = 0; i < 16; ++i) P[i] = mul2(P[i], make_float2(c, c));
-  }
-}
-
-struct ChunkOut {
-  uint32_t w[4];     // 32 packed codes
-  uint32_t sbytes;   // MX: 1 byte; NV: 2 bytes (block of lanes .x, block of lanes .y)
-  uint32_t e4[8];    // optional E4M3 bytes
-};
-
-// Scale, round and pack one rotated chunk.
-//   S_t    NV tensor scale (ignored for MX)
-//   idx0   index of element 0 in the stored copy (multiple of 32), for SR
-template <int GRID, int SCALE, int ROUND>
-__device__ __forceinline__ void quantize_chunk(float2 (&P)[16], float S_t, uint64_t idx0,
-                                               uint32_t orient, uint32_t key0, uint32_t key1,
-                                               bool emit_e4m3, uint32_t* status, ChunkOut& o) {
-  constexpr float QMAX = GridK<GRID>::kQmax;
-  // block amax (NaN-propagating)
-  float m0 = 0.0f, m1 = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    m0 = absmax_nan(m0, P[i].x);
-    m1 = absmax_nan(m1, P[i].y);
-  }
-  m0 = fabsf(m0);
-  m1 = fabsf(m1);
-  float2 vm;
-  if constexpr (SCALE == FP4Q_SCALE_MX) {
-    const float m = fabsf(absmax_nan(m0, m1));
-    const uint32_t mb = __float_as_uint(m);
-    if (mb >= 0x7F800000u) raise_status(status, FP4Q_DEV_NONFINITE);
-    int sb = (int)(mb >> 23) - GridK<GRID>::kEmax;   // floor(log2 m) - e_max + 127, 0 for m = 0
-    sb = sb < 0 ? 0 : (sb > 254 ? 254 : sb);
-    // 2^-e = 2^(127 - sb): exponent field 254 - sb, or 2^-127 (subnormal) at sb = 254
-    const float mul = (sb < 254) ? __uint_as_float((uint32_t)(254 - sb) << 23) : __uint_as_float(0x00400000u);
-    vm = make_float2(mul, mul);
-    o.sbytes = (uint32_t)sb;
-  } else {
-    if (__float_as_uint(m0) >= 0x7F800000u || __float_as_uint(m1) >= 0x7F800000u)
-      raise_status(status, FP4Q_DEV_NONFINITE);
-    uint32_t s0 = 0, s1 = 0;
-    float r0 = 0.0f, r1 = 0.0f;
-    if (S_t > 0.0f) {
-      s0 = cvt_e4m3(__fdiv_rn(__fdiv_rn(m0, QMAX), S_t));
-      s1 = cvt_e4m3(__fdiv_rn(__fdiv_rn(m1, QMAX), S_t));
-      if (s0) {
-        r0 = __frcp_rn(__fmul_rn(e4m3_to_f32(s0), S_t));
-        if (isinf(r0)) r0 = FLT_MAX;
-      }
-      if (s1) {
-        r1 = __frcp_rn(__fmul_rn(e4m3_to_f32(s1), S_t));
-        if (isinf(r1)) r1 = FLT_MAX;
-      }
-    }
-    vm = make_float2(r0, r1);   // a zero multiplier leaves sign|0 codes
-    o.sbytes = s0 | (s1 << 8);
-  }
-#pragma unroll
-  for (int i = 0; i < 16; ++i) P[i] = mul2(P[i], vm);
-
-  if constexpr (ROUND == FP4Q_RTNE && GRID != FP4Q_GRID_E1M2) {
-    o.w[0] = cvt_e2m1x8(P[0].x, P[1].x, P[2].x, P[3].x, P[4].x, P[5].x, P[6].x, P[7].x);
-    o.w[1] = cvt_e2m1x8(P[8].x, P[9].x, P[10].x, P[11].x, P[12].x, P[13].x, P[14].x, P[15].x);
-    o.w[2] = cvt_e2m1x8(P[0].y, P[1].y, P[2].y, P[3].y, P[4].y, P[5].y, P[6].y, P[7].y);
-    o.w[3] = cvt_e2m1x8(P[8].y, P[9].y, P[10].y, P[11].y, P[12].y, P[13].y, P[14].y, P[15].y);
-    if constexpr (GRID == FP4Q_GRID_E2M1_R4) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) o.w[q] = cap_e2m1_codes(o.w[q]);
-    }
-  } else if constexpr (ROUND == FP4Q_RTNE) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t w = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = (q & 1) * 8 + j;
-        const float v = (q < 2) ? P[i].x : P[i].y;
-        w |= rtne_e1m2(v) << (4 * j);
-      }
-      o.w[q] = w;
-    }
-  } else {
-    // stochastic rounding: element t of the chunk takes half (t & 1) of word
-    // (t >> 1) & 3 of Philox call t >> 3, counter (idx >> 3) of the copy.
-    const uint64_t c = idx0 >> 3;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint64_t cq = c + (uint64_t)q;
-      const Philox4 r = philox4x32_10((uint32_t)cq, (uint32_t)(cq >> 32), orient, 0u, key0, key1);
-      uint32_t w = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int t = q * 8 + j;
-        const float v = (t < 16) ? P[t].x : P[t - 16].y;
-        const float rf = r16_float((j & 1) ? (r.v[j >> 1] >> 16) : (r.v[j >> 1] & 0xFFFFu));
-        const uint32_t code = (GRID == FP4Q_GRID_E1M2) ? sr_e1m2(v, rf)
-                              : (GRID == FP4Q_GRID_E2M1_R4) ? sr_e2m1<4>(v, rf) : sr_e2m1<6>(v, rf);
-        w |= code << (4 * j);
-      }
-      o.w[q] = w;
-    }
-  }
-  if (emit_e4m3) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint2 e = codes_to_e4m3<GRID>(o.w[q]);
-      o.e4[2 * q] = e.x;
-      o.e4[2 * q + 1] = e.y;
-    }
-  }
-}
 
 // Store one quantized chunk of row `r` of a copy with `ncols` columns,
 // starting at column c0 (multiple of 32).
