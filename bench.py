@@ -307,6 +307,7 @@ def run_ours(args, world, rank, local):
     if not args.no_configs:
         del hX, hW, hdY, hY, hdX, hdW
         line["quantizer_configs"] = quant_configs(dev, stream, flush)
+        line["epilogue_fusion"] = epilogue_fusion(dev, stream, flush, X, W, cfg_x, cfg_w)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
     return line
@@ -415,6 +416,50 @@ def quant_configs(dev, stream, flush, reps: int = 20) -> dict:
               timed(lambda: fp4q.rht_quantize(x, cfg1, ro, co, stream=stream)), q_bytes(R, C, 16, 2))
     torch.cuda.synchronize(dev)
     return out
+
+
+def epilogue_fusion(dev, stream, flush, X, W, cfg_x, cfg_w, reps: int = 20) -> dict:
+    """Fprop followed by the quantization of its bf16 output for the next layer
+    (row-wise copy, random H16, MX E2M1): the two calls against the GEMM that
+    quantizes in its epilogue (no bf16 output)."""
+    import torch
+
+    from fp4_microscaled_quantization_gb300 import fp4q
+
+    Xr, _ = fp4q.rht_quantize(X, fp4q.Config(grid=cfg_x.grid, rot=16, sign_mask_row=cfg_x.sign_mask_row,
+                                             want_col=False, sf_layout=fp4q.SF_MMA), stream=stream)
+    Wr, _ = fp4q.rht_quantize(W, fp4q.Config(grid=cfg_w.grid, rot=16, sign_mask_row=cfg_w.sign_mask_row,
+                                             want_col=False, sf_layout=fp4q.SF_MMA), stream=stream)
+    M, N = Xr.rows, Wr.rows
+    ocfg = fp4q.Config(rot=16, sign_mask_row=fp4q.sign_mask_from_seed(SEED + 7, 16), want_col=False,
+                       sf_layout=fp4q.SF_MMA)
+    Y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    q1 = fp4q.alloc_operand(M, N, ocfg, dev)
+    q2 = fp4q.alloc_operand(M, N, ocfg, dev)
+
+    def timed(fn):
+        ts = []
+        for i in range(reps + 2):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            if i >= 2:
+                ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(ts)
+
+    def two_calls():
+        fp4q.gemm(Xr, Wr, fp4q.GRID_E2M1, fp4q.SCALE_MX, want_f32=False, D_bf16=Y, stream=stream)
+        fp4q.rht_quantize(Y, ocfg, q1, stream=stream)
+
+    t2 = timed(two_calls)
+    t1 = timed(lambda: fp4q.gemm_quantize(Xr, Wr, fp4q.GRID_E2M1, fp4q.SCALE_MX, ocfg, out=q2, stream=stream))
+    torch.cuda.synchronize(dev)
+    same = bool(torch.equal(q1.codes, q2.codes) and torch.equal(q1.scales, q2.scales))
+    return {"shape": f"{M}x{N}x{Xr.cols}", "gemm_then_quantize_us": round(t2, 2), "fused_us": round(t1, 2),
+            "fused_over_two_calls": round(t1 / t2, 3), "identical_copies": same}
 
 
 # ------------------------------------------------------------------ oracle arm

@@ -66,7 +66,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;      // accumulator columns [0, 256); scale columns after it
 constexpr int STG_BYTES = 4096;      // one epilogue store box (32 rows x 128 bytes)
 
-template <int KIND, bool PAIR>
+template <int KIND, bool PAIR, bool FUSED = false>
 struct KindK {
   // chunks = 512-byte groups of 4 consecutive scale bytes of one 128-row group
   static constexpr int kChunks = KIND == KIND_MXF4 ? 2 : (KIND == KIND_NVF4 ? 4 : 1);   // per K-tile
@@ -82,11 +82,14 @@ struct KindK {
   static constexpr int kSfColsA = KIND == KIND_F8 ? 4 : 4 * kChunks;
   static constexpr int kSfColsB = 8 * kChunks;
   static constexpr int kStage = (A_BYTES + kBBytes + kCompact + 1023) / 1024 * 1024;
-  static constexpr int kStagesMax = (232448 - 1280 - 4 * STG_BYTES) / kStage;
+  // epilogue staging per warp: one 32 x 64 bf16 store box, or (fused output
+  // quantization) the warp's whole 32 x 256 bf16 slice of the tile
+  static constexpr int kStgWarp = FUSED ? 4 * STG_BYTES : STG_BYTES;
+  static constexpr int kStagesMax = (232448 - 1280 - 4 * kStgWarp) / kStage;
   static constexpr int kStages = kStagesMax > 6 ? 6 : kStagesMax;
-  static constexpr int kBarOff = kStages * kStage + 4 * STG_BYTES;   // stages, then one store box per epilogue warp
+  static constexpr int kBarOff = kStages * kStage + 4 * kStgWarp;    // stages, then the epilogue staging
   static constexpr int kSmem = kBarOff + 256 + 1024;                 // + barriers + alignment slack
-  static_assert(kStages >= 3, "pipeline depth");
+  static_assert(kStages >= (FUSED ? 2 : 3), "pipeline depth");
   static_assert(kSmem <= 232448, "shared memory");
   static_assert(ACC_COL + BN + kStages * (kSfColsA + kSfColsB) <= TMEM_COLS, "tensor memory");
 };
@@ -332,7 +335,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmDh, const __grid_constant__ CUtensorMap tmDf,
                    const GemmParams p) {
-  using KK = KindK<KIND, PAIR>;
+  using KK = KindK<KIND, PAIR, (QG >= 0)>;
   constexpr int S = KK::kStages;
   constexpr int TM = PAIR ? 256 : BM;                         // tile rows
   constexpr int SFA_OFF = A_BYTES + KK::kBBytes;              // compact chunks: A, B group 0, B group 1
@@ -545,7 +548,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ---------------- epilogue (warps 2..5 -> TMEM lane quarters 2, 3, 0, 1)
     const int sp = warp & 3;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * sp) << 16) + ACC_COL;
-    const uint32_t stg = stg_base + (uint32_t)(warp - 2) * STG_BYTES;   // one store box per warp
+    const uint32_t stg = stg_base + (uint32_t)(warp - 2) * KK::kStgWarp;
     // 128B-swizzled box row `lane`: 16-byte unit u of the row sits at unit u ^ (lane & 7)
     const uint32_t row_off = 128u * (uint32_t)lane;
     const uint32_t swz = (uint32_t)(lane & 7);
@@ -567,6 +570,80 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       tc_fence_after();
       const int ncols = min(BN, p.N - n0);   // 128 or 256
+      if constexpr (QG >= 0) {
+        // Fused output quantization.  The warp's 32 x 256 bf16 slice goes to
+        // shared memory as four swizzled 32 x 64 boxes (the previous tile's
+        // stores must have read them), the accumulator is released, the boxes
+        // are stored by TMA when D is wanted, and each thread quantizes its
+        // row from them, 32 values at a time.
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncwarp();
+#pragma unroll
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          if (c0 < ncols) {
+            uint32_t r[32];
+            tmem_ld32(lane_base + (uint32_t)c0, r);
+            uint32_t hw[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              float a = __uint_as_float(r[2 * j]), b = __uint_as_float(r[2 * j + 1]);
+              if constexpr (KIND == KIND_NVF4) {
+                a = __fmul_rn(a, alpha);
+                b = __fmul_rn(b, alpha);
+              }
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(a, b);
+              hw[j] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            const uint32_t box = stg + 4096u * (uint32_t)(c0 / 64), u0 = 4u * (uint32_t)((c0 / 32) & 1);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              st_shared16(box + row_off + 16u * ((u0 + j) ^ swz), make_uint4(hw[4 * j], hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (PAIR) remote_arrive(lead_acc_empty);
+          else mbar_arrive(lead_acc_empty);
+        }
+        if (!live) continue;
+        if (p.want_bf16) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            for (int b = 0; 64 * b < ncols; ++b) tma_store_2d(&tmDh, n0 + 64 * b, y, stg + 4096u * (uint32_t)b);
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          }
+        }
+        const int64_t row = (int64_t)y + lane;
+#pragma unroll 1
+        for (int c0 = 0; c0 < ncols; c0 += 32) {
+          const uint32_t box = stg + 4096u * (uint32_t)(c0 / 64), u0 = 4u * (uint32_t)((c0 / 32) & 1);
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 v = chunk_row(box + row_off + 16u * ((u0 + j) ^ swz), 0);
+            w[4 * j] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
+          }
+          float2 P[16];
+          chunk_from_bf16_words(w, p.q_sgn, P);
+          if (p.q_nh == 16) rotate_chunk<16>(P);
+          else if (p.q_nh == 32) rotate_chunk<32>(P);
+          ChunkOut o;
+          const int64_t col = (int64_t)n0 + c0;
+          quantize_chunk<QG, FP4Q_SCALE_MX, QR>(P, 0.0f, (uint64_t)(row * p.N + col), 0u, (uint32_t)p.q_seed,
+                                                (uint32_t)(p.q_seed >> 32), p.q_e4m3 != nullptr, p.status, o);
+          *reinterpret_cast<uint4*>(p.q_codes + row * (p.N / 2) + col / 2) = make_uint4(o.w[0], o.w[1], o.w[2], o.w[3]);
+          const int64_t nkb = p.N / 32, k = col / 32;
+          p.q_scales[p.q_sf_mma ? sf_mma_offset(row, k, nkb) : row * nkb + k] = (uint8_t)o.sbytes;
+          if (p.q_e4m3) {
+            uint4* ep = reinterpret_cast<uint4*>(p.q_e4m3 + row * p.N + col);
+            ep[0] = make_uint4(o.e4[0], o.e4[1], o.e4[2], o.e4[3]);
+            ep[1] = make_uint4(o.e4[4], o.e4[5], o.e4[6], o.e4[7]);
+          }
+        }
+        continue;
+      }
       uint32_t h[BN / 2];                    // the row as packed bf16
 #pragma unroll
       for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -596,30 +673,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int j = 0; j < 16; ++j) {
             const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
             h[c0 / 2 + j] = *reinterpret_cast<const uint32_t*>(&b2);
-          }
-          if constexpr (QG >= 0) {
-            // quantize this row's 32 bf16 outputs as the next operand's row-wise chunk
-            if (live) {
-              uint32_t w[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j) w[j] = h[c0 / 2 + j];
-              float2 P[16];
-              chunk_from_bf16_words(w, p.q_sgn, P);
-              if (p.q_nh == 16) rotate_chunk<16>(P);
-              else if (p.q_nh == 32) rotate_chunk<32>(P);
-              ChunkOut o;
-              const int64_t row = (int64_t)y + lane, col = (int64_t)n0 + c0;
-              quantize_chunk<QG, FP4Q_SCALE_MX, QR>(P, 0.0f, (uint64_t)(row * p.N + col), 0u, (uint32_t)p.q_seed,
-                                                    (uint32_t)(p.q_seed >> 32), p.q_e4m3 != nullptr, p.status, o);
-              *reinterpret_cast<uint4*>(p.q_codes + row * (p.N / 2) + col / 2) = make_uint4(o.w[0], o.w[1], o.w[2], o.w[3]);
-              const int64_t nkb = p.N / 32, k = col / 32;
-              p.q_scales[p.q_sf_mma ? sf_mma_offset(row, k, nkb) : row * nkb + k] = (uint8_t)o.sbytes;
-              if (p.q_e4m3) {
-                uint4* ep = reinterpret_cast<uint4*>(p.q_e4m3 + row * p.N + col);
-                ep[0] = make_uint4(o.e4[0], o.e4[1], o.e4[2], o.e4[3]);
-                ep[1] = make_uint4(o.e4[4], o.e4[5], o.e4[6], o.e4[7]);
-              }
-            }
           }
         }
       }
@@ -683,7 +736,7 @@ bool make_out_map(CUtensorMap* m, const void* base, uint64_t N, uint64_t M, bool
 template <int KIND, bool PAIR, int QG = -1, int QR = FP4Q_RTNE>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& dh, const CUtensorMap& df,
                         const GemmParams& p, cudaStream_t s) {
-  using KK = KindK<KIND, PAIR>;
+  using KK = KindK<KIND, PAIR, (QG >= 0)>;
   static unsigned attr_set = 0;   // one bit per device ordinal < 32
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
         L.fp4q_dequantize.argtypes = [P, i64, i64, P, i32, i32, P, P]
         L.fp4q_gemm.restype = i32
         L.fp4q_gemm.argtypes = [P, P, i64, i64, i64, i32, i32, P, P, P, P]
+        L.fp4q_gemm_quantize.restype = i32
+        L.fp4q_gemm_quantize.argtypes = [P, P, i64, i64, i64, i32, i32, P, P, P, P, P]
         L.fp4q_bias_stats_workspace_bytes.restype = sz
         L.fp4q_bias_stats_workspace_bytes.argtypes = [i64]
         L.fp4q_bias_stats.restype = i32
@@ -234,6 +236,24 @@ def gemm(A: Operand, B: Operand, grid: int, scale: int, want_bf16: bool = True, 
     _check("fp4q_gemm", lib().fp4q_gemm(ctypes.byref(ac), ctypes.byref(bc), M, N, K, grid, scale, _p(D_bf16),
                                          _p(D_f32), _p(status), _stream(stream)))
     return D_bf16, D_f32
+
+
+def gemm_quantize(A: Operand, B: Operand, grid: int, scale: int, out_cfg: Config, want_bf16: bool = False,
+                  D_bf16=None, out: Operand | None = None, status=None, stream=None):
+    """D = alpha_g * A B^T with the row-wise copy of bf16(D) under out_cfg made in
+    the GEMM's epilogue.  Returns (D_bf16 or None, out)."""
+    M, K = A.rows, A.cols
+    N = B.rows
+    dev = A.codes.device
+    if want_bf16 and D_bf16 is None:
+        D_bf16 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    if out is None:
+        out = alloc_operand(M, N, out_cfg, dev)
+    ac, bc, oc, cc = A.c(), B.c(), out.c(), out_cfg.c()
+    _check("fp4q_gemm_quantize", lib().fp4q_gemm_quantize(
+        ctypes.byref(ac), ctypes.byref(bc), M, N, K, grid, scale, _p(D_bf16), ctypes.byref(cc), ctypes.byref(oc),
+        _p(status), _stream(stream)))
+    return D_bf16, out
 
 
 def bias_stats_workspace_bytes(n: int) -> int:

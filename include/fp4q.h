@@ -181,13 +181,37 @@ int32_t fp4q_dequantize(const fp4q_operand* q, int64_t rows, int64_t cols,
  *           kind::mxf4nvf4 with E4M3 scales, E1M2+MX runs kind::mxf8f6f4 on the
  *           E4M3 bytes (E1M2 levels are exact in E4M3).  E1M2+NV is
  *           FP4Q_ERR_UNSUPPORTED.  alpha_g = S_t(A) * S_t(B) for NV, else 1.
- *  M % 128 == 0, N % 16 == 0, K % 128 == 0 (K % 64 for NV), all > 0
+ *  M % 128 == 0, N % 128 == 0, K % 128 == 0 (K % 64 for NV), all > 0
  *  D_bf16   device bf16 M x N (row-major), or NULL
  *  D_f32    device fp32 M x N, or NULL (at least one output)
  *  d_status device uint32 for FP4Q_DEV_TIMEOUT, or NULL */
 int32_t fp4q_gemm(const fp4q_operand* A, const fp4q_operand* B, int64_t M, int64_t N, int64_t K,
                   int32_t grid, int32_t scale, void* D_bf16, float* D_f32, uint32_t* d_status,
                   void* stream);
+
+/* The same GEMM, quantizing its own output in the epilogue: `out` receives
+ * the row-wise copy of bf16(D) that fp4q_rht_quantize would produce from the
+ * stored bf16 D with `out_cfg`, bit for bit, without D making a round trip
+ * through HBM.  This is the step after the hot path that the linear-layer
+ * recipe uses between layers: Fprop's Y becomes the next layer's X, Dgrad's dX
+ * the previous layer's dY ("Repensando o Vies de Encolhimento", Metodologia 2:
+ * every GEMM operand quantized, with the rotation, RTNE on activations and
+ * weights and SR on gradients).
+ *  A, B, M, N, K, grid, scale, d_status   as fp4q_gemm
+ *  D_bf16   device bf16 M x N, or NULL (the output is then only quantized)
+ *  out_cfg  the copy's recipe: grid, rot and sign_mask_row (along N, the next
+ *           GEMM's contraction axis), round and sr_seed (element index = r*N + c
+ *           of the M x N copy, orientation 0), sf_layout, emit_e4m3.  It must
+ *           ask for MX scales and the row-wise copy only (want_row = 1,
+ *           want_col = 0); NV scaling needs the amax of the whole rotated
+ *           output before the first block is encoded and is FP4Q_ERR_UNSUPPORTED,
+ *           as is a column-wise copy.
+ *  out      device copy: codes M x N/2 (16-byte aligned), scales M x N/32,
+ *           e4m3 M x N when emit_e4m3
+ * Non-finite GEMM outputs set FP4Q_DEV_NONFINITE in *d_status. */
+int32_t fp4q_gemm_quantize(const fp4q_operand* A, const fp4q_operand* B, int64_t M, int64_t N, int64_t K,
+                           int32_t grid, int32_t scale, void* D_bf16, const fp4q_config* out_cfg,
+                           fp4q_operand* out, uint32_t* d_status, void* stream);
 
 /* Bias statistics over n element pairs ([SB] Metodologia 1: attenuation
  * alpha = <approx, ref>/||ref||^2 and the magnitude shrinkage; Resultados:
