@@ -235,6 +235,11 @@ def run_ours(args, world, rank, local):
             (kq if kind == "q" else kg)[key].append(t)
     q_s = sum(q_times) / len(q_times)
     g_s = sum(g_times) / len(g_times)
+
+    def pct(v):
+        v = sorted(v)
+        return {"p10_us": round(v[len(v) // 10] * 1e6, 2), "median_us": round(v[len(v) // 2] * 1e6, 2),
+                "p90_us": round(v[(9 * len(v)) // 10] * 1e6, 2)}
     value = aggregate(q_bytes, q_s, world, dev) / 1e9
     gemm_tflops = aggregate(flops, g_s, world, dev) / 1e12
 
@@ -290,10 +295,12 @@ def run_ours(args, world, rank, local):
         "config": {"workload": WORKLOAD, "global_batch_tokens": TOKENS * world, "per_rank": "replica",
                    "l2": "flushed (256 MiB write) before every timed step", "recipe": "E2M1 MXFP4 H16"},
         "hbm_frac": round(value / world / hbm_peak, 4),
-        "quantize": {"us_per_step": round(q_s * 1e6, 2), "gb_s": round(value, 1),
+        "inputs_sha256": {"X": synth.sha256(Xb), "W": synth.sha256(Wb), "dY": synth.sha256(dYb)},
+        "quantize": {"us_per_step": round(q_s * 1e6, 2), "gb_s": round(value, 1), "spread": pct(q_times),
                      "bytes_per_step": q_bytes, "per_tensor_us": {k: round(statistics.mean(v) * 1e6, 2)
                                                                   for k, v in kq.items()}},
         "gemm": {"tflops": round(gemm_tflops, 1), "us_per_step": round(g_s * 1e6, 2), "flops_per_step": flops,
+                 "spread": pct(g_times),
                  "per_gemm_us": {k: round(statistics.mean(v) * 1e6, 2) for k, v in kg.items()}},
         "roofline": roof_gemm if dominant_gemm else roof_q,
         "roofline_other": roof_q if dominant_gemm else roof_gemm,
@@ -308,6 +315,7 @@ def run_ours(args, world, rank, local):
         del hX, hW, hdY, hY, hdX, hdW
         line["quantizer_configs"] = quant_configs(dev, stream, flush)
         line["epilogue_fusion"] = epilogue_fusion(dev, stream, flush, X, W, cfg_x, cfg_w)
+        line["recipe_quality"] = recipe_quality(X, W, dY)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
     return line
@@ -460,6 +468,20 @@ def epilogue_fusion(dev, stream, flush, X, W, cfg_x, cfg_w, reps: int = 20) -> d
     same = bool(torch.equal(q1.codes, q2.codes) and torch.equal(q1.scales, q2.scales))
     return {"shape": f"{M}x{N}x{Xr.cols}", "gemm_then_quantize_us": round(t2, 2), "fused_us": round(t1, 2),
             "fused_over_two_calls": round(t1 / t2, 3), "identical_copies": same}
+
+
+def recipe_quality(X, W, dY) -> dict:
+    """Output SQNR (dB), attenuation alpha and shrinkage of Fprop, Dgrad and Wgrad
+    under the UFP4 and E2M1 recipes, against fp32 GEMMs of the bf16 originals."""
+    from fp4_microscaled_quantization_gb300 import linear
+
+    ref = linear.reference_gemms(X, W, dY)
+    out = {}
+    for recipe in linear.RECIPES:
+        res = linear.Fp4Linear(recipe, seed=SEED, out_f32=True)(X, W, dY)
+        q = linear.output_quality(res, ref)
+        out[recipe] = {k: {m: round(v[m], 5) for m in ("sqnr_db", "alpha", "shrinkage")} for k, v in q.items()}
+    return out
 
 
 # ------------------------------------------------------------------ oracle arm

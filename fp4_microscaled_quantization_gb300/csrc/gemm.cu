@@ -615,31 +615,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
           }
         }
-        const int64_t row = (int64_t)y + lane;
-#pragma unroll 1
-        for (int c0 = 0; c0 < ncols; c0 += 32) {
-          const uint32_t box = stg + 4096u * (uint32_t)(c0 / 64), u0 = 4u * (uint32_t)((c0 / 32) & 1);
-          uint32_t w[16];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 v = chunk_row(box + row_off + 16u * ((u0 + j) ^ swz), 0);
-            w[4 * j] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
-          }
-          float2 P[16];
-          chunk_from_bf16_words(w, p.q_sgn, P);
-          if (p.q_nh == 16) rotate_chunk<16>(P);
-          else if (p.q_nh == 32) rotate_chunk<32>(P);
-          ChunkOut o;
-          const int64_t col = (int64_t)n0 + c0;
-          quantize_chunk<QG, FP4Q_SCALE_MX, QR>(P, 0.0f, (uint64_t)(row * p.N + col), 0u, (uint32_t)p.q_seed,
-                                                (uint32_t)(p.q_seed >> 32), p.q_e4m3 != nullptr, p.status, o);
-          *reinterpret_cast<uint4*>(p.q_codes + row * (p.N / 2) + col / 2) = make_uint4(o.w[0], o.w[1], o.w[2], o.w[3]);
-          const int64_t nkb = p.N / 32, k = col / 32;
-          p.q_scales[p.q_sf_mma ? sf_mma_offset(row, k, nkb) : row * nkb + k] = (uint8_t)o.sbytes;
-          if (p.q_e4m3) {
-            uint4* ep = reinterpret_cast<uint4*>(p.q_e4m3 + row * p.N + col);
-            ep[0] = make_uint4(o.e4[0], o.e4[1], o.e4[2], o.e4[3]);
-            ep[1] = make_uint4(o.e4[4], o.e4[5], o.e4[6], o.e4[7]);
+        if constexpr (QG >= 0) {
+          const int64_t row = (int64_t)y + lane;
+  #pragma unroll 1
+          for (int c0 = 0; c0 < ncols; c0 += 32) {
+            const uint32_t box = stg + 4096u * (uint32_t)(c0 / 64), u0 = 4u * (uint32_t)((c0 / 32) & 1);
+            uint32_t w[16];
+  #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 v = chunk_row(box + row_off + 16u * ((u0 + j) ^ swz), 0);
+              w[4 * j] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
+            }
+            float2 P[16];
+            chunk_from_bf16_words(w, p.q_sgn, P);
+            if (p.q_nh == 16) rotate_chunk<16>(P);
+            else if (p.q_nh == 32) rotate_chunk<32>(P);
+            ChunkOut o;
+            const int64_t col = (int64_t)n0 + c0;
+            quantize_chunk<QG, FP4Q_SCALE_MX, QR>(P, 0.0f, (uint64_t)(row * p.N + col), 0u, (uint32_t)p.q_seed,
+                                                  (uint32_t)(p.q_seed >> 32), p.q_e4m3 != nullptr, p.status, o);
+            *reinterpret_cast<uint4*>(p.q_codes + row * (p.N / 2) + col / 2) = make_uint4(o.w[0], o.w[1], o.w[2], o.w[3]);
+            const int64_t nkb = p.N / 32, k = col / 32;
+            p.q_scales[p.q_sf_mma ? sf_mma_offset(row, k, nkb) : row * nkb + k] = (uint8_t)o.sbytes;
+            if (p.q_e4m3) {
+              uint4* ep = reinterpret_cast<uint4*>(p.q_e4m3 + row * p.N + col);
+              ep[0] = make_uint4(o.e4[0], o.e4[1], o.e4[2], o.e4[3]);
+              ep[1] = make_uint4(o.e4[4], o.e4[5], o.e4[6], o.e4[7]);
+            }
           }
         }
         continue;
