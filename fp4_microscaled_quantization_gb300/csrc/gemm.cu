@@ -81,17 +81,23 @@ struct KindK {
   // TMEM scale columns per stage: A 8 per two chunks (F8: 4 for its one chunk), B 8 per chunk
   static constexpr int kSfColsA = KIND == KIND_F8 ? 4 : 4 * kChunks;
   static constexpr int kSfColsB = 8 * kChunks;
+  // columns per stage, padded so that one scale writer stores a stage with one
+  // (two for NV) 32x32b.x32 store, or one x16 for F8
+  static constexpr int kSfCols = KIND == KIND_MXF4 ? 32 : (KIND == KIND_NVF4 ? 64 : 16);
   static constexpr int kStage = (A_BYTES + kBBytes + kCompact + 1023) / 1024 * 1024;
   // epilogue staging per warp: one 32 x 64 bf16 store box, or (fused output
   // quantization) the warp's whole 32 x 256 bf16 slice of the tile
   static constexpr int kStgWarp = FUSED ? 4 * STG_BYTES : STG_BYTES;
   static constexpr int kStagesMax = (232448 - 1280 - 4 * kStgWarp) / kStage;
-  static constexpr int kStages = kStagesMax > 6 ? 6 : kStagesMax;
+  static constexpr int kStagesCap = kStagesMax > 6 ? 6 : kStagesMax;
+  static constexpr int kStagesTmem = (int)(TMEM_COLS - BN) / kSfCols;   // stages whose scales fit beside the accumulator
+  static constexpr int kStages = kStagesCap > kStagesTmem ? kStagesTmem : kStagesCap;
   static constexpr int kBarOff = kStages * kStage + 4 * kStgWarp;    // stages, then the epilogue staging
   static constexpr int kSmem = kBarOff + 256 + 1024;                 // + barriers + alignment slack
   static_assert(kStages >= (FUSED ? 2 : 3), "pipeline depth");
   static_assert(kSmem <= 232448, "shared memory");
-  static_assert(ACC_COL + BN + kStages * (kSfColsA + kSfColsB) <= TMEM_COLS, "tensor memory");
+  static_assert(kSfColsA + kSfColsB <= kSfCols, "scale columns");
+  static_assert(ACC_COL + BN + kStages * kSfCols <= TMEM_COLS, "tensor memory");
 };
 
 struct GemmParams {
@@ -222,16 +228,30 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-// This warp's TMEM lane quarter, 8 (4) consecutive 32-bit columns from taddr.
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, uint4 a, uint4 b) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
-               ::"r"(taddr), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
-               : "memory");
+// This warp's TMEM lane quarter, 32 (16) consecutive 32-bit columns from taddr.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* w) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+      ::"r"(taddr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+        "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]),
+        "r"(w[16]), "r"(w[17]), "r"(w[18]), "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]),
+        "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]), "r"(w[28]), "r"(w[29]), "r"(w[30]), "r"(w[31])
+      : "memory");
 }
-__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint4 a) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
-               ::"r"(taddr), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w)
-               : "memory");
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* w) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};"
+      ::"r"(taddr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+        "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
+      : "memory");
+}
+__device__ __forceinline__ void put4(uint32_t* w, uint4 v) {
+  w[0] = v.x;
+  w[1] = v.y;
+  w[2] = v.z;
+  w[3] = v.w;
 }
 // 16-byte row i of a compact chunk (rows 0..31 of the 512-byte chunk).
 __device__ __forceinline__ uint4 chunk_row(uint32_t chunk, int i) {
@@ -339,7 +359,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   constexpr int S = KK::kStages;
   constexpr int TM = PAIR ? 256 : BM;                         // tile rows
   constexpr int SFA_OFF = A_BYTES + KK::kBBytes;              // compact chunks: A, B group 0, B group 1
-  constexpr uint32_t SF_COLS = KK::kSfColsA + KK::kSfColsB;   // per stage
+  constexpr uint32_t SF_COLS = KK::kSfCols;                   // per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -521,16 +541,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t ca = st + SFA_OFF, cb0 = ca + KK::kChunks * 512, cb1 = cb0 + KK::kChunks * 512;
         const uint32_t sfa_col = qbase + ACC_COL + BN + SF_COLS * (uint32_t)s;
         const uint32_t sfb_col = sfa_col + KK::kSfColsA;
-        if constexpr (KIND == KIND_F8) {
-          tmem_st4(sfa_col, chunk_row(ca, lane));
-        } else {
+        // the stage's columns in order: A chunks (4 each), then per B chunk its two row groups
+        uint32_t w[KK::kSfCols];
 #pragma unroll
-          for (int pr = 0; pr < KK::kChunks / 2; ++pr)
-            tmem_st8(sfa_col + 8 * pr, chunk_row(ca + 1024u * pr, lane), chunk_row(ca + 1024u * pr + 512u, lane));
+        for (int c = 0; c < KK::kChunks; ++c) put4(w + 4 * c, chunk_row(ca + 512u * c, lane));
+#pragma unroll
+        for (int c = 0; c < KK::kChunks; ++c) {
+          put4(w + KK::kSfColsA + 8 * c, chunk_row(cb0 + 512u * c, lane));
+          put4(w + KK::kSfColsA + 8 * c + 4, chunk_row(cb1 + 512u * c, lane));
         }
 #pragma unroll
-        for (int c = 0; c < KK::kChunks; ++c)
-          tmem_st8(sfb_col + 8 * c, chunk_row(cb0 + 512u * c, lane), chunk_row(cb1 + 512u * c, lane));
+        for (int j = KK::kSfColsA + KK::kSfColsB; j < KK::kSfCols; ++j) w[j] = 0u;
+        if constexpr (KK::kSfCols == 16) {
+          tmem_st16(sfa_col, w);
+        } else {
+#pragma unroll
+          for (int h = 0; h < KK::kSfCols / 32; ++h) tmem_st32(sfa_col + 32 * h, w + 32 * h);
+        }
+        (void)sfb_col;
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
