@@ -206,23 +206,24 @@ __device__ __forceinline__ void read_row_chunk(const TileView& tv, int r, int q,
   // word k holds elements 2k (low half) and 2k+1 (high half)
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    P[2 * k].x = __uint_as_float((w[k] << 16) ^ sgn[2 * k]);
+    P[2 * k].x = __uint_as_float(w[k] * 65536u + sgn[2 * k]);
     P[2 * k + 1].x = __uint_as_float((w[k] & 0xFFFF0000u) ^ sgn[2 * k + 1]);
-    P[2 * k].y = __uint_as_float((w[k + 8] << 16) ^ sgn[2 * k + 16]);
+    P[2 * k].y = __uint_as_float(w[k + 8] * 65536u + sgn[2 * k + 16]);
     P[2 * k + 1].y = __uint_as_float((w[k + 8] & 0xFFFF0000u) ^ sgn[2 * k + 17]);
   }
 }
 
 // Column c (0..255) of the tile's 32 rows as pairs with the signs applied.
-// A word holds columns 2p (low half) and 2p+1 (high half); one byte permute
-// moves this thread's half to the top and clears the rest.
+// A word holds columns 2p (low half) and 2p+1 (high half); an integer multiply
+// (by 65536 for the low half, by 1 for the high half) brings this thread's
+// half to the top and the mask clears the rest.
 __device__ __forceinline__ void read_col_chunk(const TileView& tv, int c, const uint32_t* sgn, float2 (&P)[16]) {
-  const uint32_t sel = (c & 1) ? 0x3244u : 0x1044u;
+  const uint32_t mul = (c & 1) ? 1u : 65536u;   // brings this thread's half of a word to the top
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const uint32_t a = tv.word(i, c >> 1), b = tv.word(i + 16, c >> 1);
-    P[i].x = __uint_as_float(__byte_perm(a, 0u, sel) ^ sgn[i]);
-    P[i].y = __uint_as_float(__byte_perm(b, 0u, sel) ^ sgn[i + 16]);
+    P[i].x = __uint_as_float(((a * mul) & 0xFFFF0000u) ^ sgn[i]);
+    P[i].y = __uint_as_float(((b * mul) & 0xFFFF0000u) ^ sgn[i + 16]);
   }
 }
 

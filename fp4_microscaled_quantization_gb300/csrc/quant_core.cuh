@@ -136,14 +136,16 @@ __device__ __forceinline__ void rotate_chunk(float2 (&P)[16]) {
 
 // A chunk of 32 bf16 values given as 16 words (word k holds elements 2k in
 // its low half and 2k+1 in its high half), widened to fp32 pairs
-// P[i] = (u[i], u[i+16]) with the sign words applied.
+// P[i] = (u[i], u[i+16]) with the sign words applied.  For a low half,
+// w * 65536 + sign equals (w << 16) ^ sign (the sign word only has bit 31 and
+// the low 16 bits are zero) and is one multiply-add.
 __device__ __forceinline__ void chunk_from_bf16_words(const uint32_t (&w)[16], const uint32_t* sgn,
                                                       float2 (&P)[16]) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    P[2 * k].x = __uint_as_float((w[k] << 16) ^ sgn[2 * k]);
+    P[2 * k].x = __uint_as_float(w[k] * 65536u + sgn[2 * k]);
     P[2 * k + 1].x = __uint_as_float((w[k] & 0xFFFF0000u) ^ sgn[2 * k + 1]);
-    P[2 * k].y = __uint_as_float((w[k + 8] << 16) ^ sgn[2 * k + 16]);
+    P[2 * k].y = __uint_as_float(w[k + 8] * 65536u + sgn[2 * k + 16]);
     P[2 * k + 1].y = __uint_as_float((w[k + 8] & 0xFFFF0000u) ^ sgn[2 * k + 17]);
   }
 }
