@@ -1,5 +1,5 @@
 """Parity at the full workload sizes, in the launch configuration the benchmark
-times (64 x 256 quantizer tiles, 128 x 256 GEMM tiles):
+times (32 x 256 quantizer tiles, 128 x 256 GEMM tiles):
 
   tiny    X 256x512, row-wise, H16 + seeded signs, MX E2M1 and E1M2, RTNE, with
           SQNR / shrinkage of the reconstruction
