@@ -238,8 +238,14 @@ __device__ __forceinline__ void row_task(int t, int& r, int& q) {
 // Per tile each thread quantizes one column chunk (32 rows of one column, the
 // column-wise copy) and one row chunk (32 columns of one row, the row-wise
 // copy).
+// Resident CTAs per SM: stochastic rounding runs Philox and the exact
+// round-up decision per element and does better with the register budget of
+// two CTAs per SM; the other modes with three.
+template <int ROUND>
+constexpr int quant_ctas() { return ROUND == FP4Q_SR ? 2 : QUANT_MIN_CTAS; }
+
 template <int GRID, int SCALE, int NH, int ROUND>
-__global__ void __launch_bounds__(kNT, QUANT_MIN_CTAS)
+__global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
     rht_quant_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
   const uint32_t key0 = (uint32_t)p.sr_seed, key1 = (uint32_t)(p.sr_seed >> 32);
   constexpr float kDen = 448.0f * GridK<GRID>::kQmax;
@@ -473,9 +479,9 @@ static bool input_map(const QuantParams& p, CUtensorMap* m) {
                         (uint64_t)p.ld * 2u, 64u, (uint32_t)kTR, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-static unsigned persistent_grid(const QuantParams& p) {
+static unsigned persistent_grid(const QuantParams& p, int ctas_per_sm = QUANT_MIN_CTAS) {
   const int64_t ntiles = ((p.cols + kTC - 1) / kTC) * ((p.rows + kTR - 1) / kTR);
-  const int64_t g = QUANT_MIN_CTAS * (int64_t)num_sms();
+  const int64_t g = ctas_per_sm * (int64_t)num_sms();
   return (unsigned)(ntiles < g ? ntiles : g);
 }
 
@@ -493,7 +499,7 @@ static cudaError_t launch_quant_inst(const CUtensorMap& m, const QuantParams& p,
   static bool attr = false;
   cudaError_t e = smem_attr(rht_quant_kernel<GRID, SCALE, NH, ROUND>, attr);
   if (e != cudaSuccess) return e;
-  rht_quant_kernel<GRID, SCALE, NH, ROUND><<<persistent_grid(p), kNT, kQuantSmem, s>>>(m, p);
+  rht_quant_kernel<GRID, SCALE, NH, ROUND><<<persistent_grid(p, quant_ctas<ROUND>()), kNT, kQuantSmem, s>>>(m, p);
   return cudaGetLastError();
 }
 
