@@ -442,17 +442,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const int nch = min(KK::kChunks, nq - q0);
           const uint32_t sf_bytes = (uint32_t)nch * 512u;
           const uint32_t st = sbase + (uint32_t)s * KK::kStage;
-          const uint32_t fb = lead_full + 8 * s, sb = bar_sfd + 8 * s;
+          // the scale chunks complete on this CTA's own barrier: the full barrier
+          // itself for a single CTA, a separate one in a pair (whose full
+          // barrier lives in the leader)
+          const uint32_t fb = lead_full + 8 * s, sb = PAIR ? bar_sfd + 8 * s : bar_full + 8 * s;
+          const uint32_t sf_tx = sf_bytes * ((rows ? 1u : 0u) + (rg1 ? 2u : 1u));
           if constexpr (PAIR) {
             remote_expect_tx(fb, A_BYTES + KK::kBBytes);
             tma_load_2d_pair(st, &tmA, kt * KROW, m0, fb);
             tma_load_2d_pair(st + A_BYTES, &tmB, kt * KROW, n0 + 128 * (int)rank, fb);
           } else {
-            mbar_expect_tx(fb, A_BYTES + KK::kBBytes);
+            mbar_expect_tx(fb, A_BYTES + KK::kBBytes + sf_tx);
             tma_load_2d(st, &tmA, kt * KROW, m0, fb);
             tma_load_2d(st + A_BYTES, &tmB, kt * KROW, n0, fb);
           }
-          mbar_expect_tx(sb, sf_bytes * ((rows ? 1u : 0u) + (rg1 ? 2u : 1u)));
+          if constexpr (PAIR) mbar_expect_tx(sb, sf_tx);
           if (rows) bulk_load(st + SFA_OFF, p.sfa + ((size_t)(m0 / 128) * nq + q0) * 512, sf_bytes, sb);
           bulk_load(st + SFA_OFF + KK::kChunks * 512, p.sfb + ((size_t)(n0 / 128) * nq + q0) * 512, sf_bytes, sb);
           if (rg1)
@@ -474,7 +478,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int kt = 0; kt < num_kt; ++kt, ++it) {
           const int s = (int)(it % S);
           const uint32_t ph = (it / S) & 1u;
-          ok = mbar_wait(bar_full + 8 * s, ph, abort_flag) && mbar_wait(bar_sf + 8 * s, ph, abort_flag);
+          // single CTA: the scale writers arrive on bar_sf only after the
+          // stage's full barrier completed, so bar_sf alone orders the operands too
+          if constexpr (PAIR) ok = mbar_wait(bar_full + 8 * s, ph, abort_flag) && mbar_wait(bar_sf + 8 * s, ph, abort_flag);
+          else ok = mbar_wait(bar_sf + 8 * s, ph, abort_flag);
           if (!ok) break;
           tc_fence_after();
           const uint32_t st = sbase + (uint32_t)s * KK::kStage;
@@ -482,7 +489,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const uint32_t sfb_col = sfa_col + KK::kSfColsA;
           const int rem = p.K - kt * KK::kElemsPerTile;
           const int n_mma = min(4, rem / KK::kMmaK);
-          for (int k = 0; k < n_mma; ++k) {
+          // descriptors of K slice k: the start address field advances by 32 bytes (2 units of 16)
+          const uint64_t da = op_desc(st), db = op_desc(st + A_BYTES);
+          const uint32_t acc0 = kt > 0 ? 1u : 0u;
+          auto issue = [&](int k) {
             uint32_t sfa = sfa_col, sfb = sfb_col, sf_id = 0;
             if constexpr (KIND == KIND_MXF4) {
               sfa += 4 * (k >> 1);
@@ -494,13 +504,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             } else {
               sf_id = (uint32_t)k;
             }
-            const uint32_t acc = (kt > 0 || k > 0) ? 1u : 0u;
+            const uint32_t acc = k > 0 ? 1u : acc0;
             if constexpr (PAIR)
-              tc_mma_pair<KIND>(tmem + ACC_COL, op_desc(st + 32 * k), op_desc(st + A_BYTES + 32 * k),
-                                make_idesc<KIND, TM>(sf_id), sfa, sfb, acc);
+              tc_mma_pair<KIND>(tmem + ACC_COL, da + 2u * k, db + 2u * k, make_idesc<KIND, TM>(sf_id), sfa, sfb, acc);
             else
-              tc_mma<KIND>(tmem + ACC_COL, op_desc(st + 32 * k), op_desc(st + A_BYTES + 32 * k),
-                           make_idesc<KIND, TM>(sf_id), sfa, sfb, acc);
+              tc_mma<KIND>(tmem + ACC_COL, da + 2u * k, db + 2u * k, make_idesc<KIND, TM>(sf_id), sfa, sfb, acc);
+          };
+          if (n_mma == 4) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) issue(k);
+          } else {
+            for (int k = 0; k < n_mma; ++k) issue(k);
           }
           if constexpr (PAIR) tc_commit_pair(bar_empty + 8 * s);
           else tc_commit(bar_empty + 8 * s);
@@ -533,7 +547,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int kt = 0; kt < num_kt; ++kt, ++it) {
         const int s = (int)(it % S);
         const uint32_t ph = (it / S) & 1u;
-        ok = mbar_wait(bar_sfd + 8 * s, ph, abort_flag);
+        ok = mbar_wait(PAIR ? bar_sfd + 8 * s : bar_full + 8 * s, ph, abort_flag);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) break;
         tc_fence_after();
