@@ -56,6 +56,8 @@ namespace fp4q {
 namespace {
 
 enum { KIND_MXF4 = 0, KIND_NVF4 = 1, KIND_F8 = 2 };
+// CTA cooperation: none, a cta_group::2 pair, or a cluster of two that shares B by TMA multicast
+enum { CL_SINGLE = 0, CL_PAIR = 1, CL_MC = 2 };
 
 constexpr int BM = 128;              // accumulator rows per CTA (TMEM lanes)
 constexpr int BN = 256;              // tile columns (MMA N)
@@ -317,6 +319,24 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
       "h"((uint16_t)3)
       : "memory");
 }
+// TMA load delivered to the same shared-memory offset, and completing on the
+// barrier at the same offset, in both CTAs of the cluster.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* tm, int32_t x, int32_t y,
+                                               uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
+      "[%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(tm), "r"(x), "r"(y), "r"(bar), "h"((uint16_t)3)
+      : "memory");
+}
+// Commit of this CTA's tensor-core work, arriving on the barrier at this
+// offset in both CTAs of the cluster.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
 template <int KIND>
 __device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
                                             uint32_t sfb, uint32_t acc) {
@@ -349,15 +369,23 @@ __device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, 
 // 128r..128r+127 of the tile's B, and tcgen05.mma.cta_group::2 issued by rank
 // 0 (the leader) reads both CTAs' operands, so each SM moves 32 KB of A/B per
 // K-tile instead of 48 KB and its tensor core reads half of B from the peer.
+// Multicast cluster (CL_MC, clusters of two): the same 256 x 256 tiles, but
+// each CTA runs its own cta_group::1 MMAs on a full copy of B in its shared
+// memory; rank r loads B rows 128r..128r+127 once and TMA multicast writes
+// them into both CTAs, so each SM pulls 32 KB of A/B per K-tile out of L2.
+// A stage's ring slot is refilled only after both CTAs' MMAs released it:
+// every commit arrives on the empty barrier of both CTAs.
 // Tile id -> (m block = id / n_blocks, n block = id % n_blocks).
-template <int KIND, bool PAIR, int QG = -1, int QR = FP4Q_RTNE>
+template <int KIND, int CL, int QG = -1, int QR = FP4Q_RTNE>
 __global__ void __launch_bounds__(NTHREADS, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmDh, const __grid_constant__ CUtensorMap tmDf,
                    const GemmParams p) {
+  constexpr bool PAIR = CL == CL_PAIR, MC = CL == CL_MC, CLU = CL != CL_SINGLE;
   using KK = KindK<KIND, PAIR, (QG >= 0)>;
   constexpr int S = KK::kStages;
-  constexpr int TM = PAIR ? 256 : BM;                         // tile rows
+  constexpr int TM = CLU ? 256 : BM;                          // tile rows
+  constexpr int MMA_M = PAIR ? 256 : BM;                      // rows of one MMA (both CTAs' in a pair)
   constexpr int SFA_OFF = A_BYTES + KK::kBBytes;              // compact chunks: A, B group 0, B group 1
   constexpr uint32_t SF_COLS = KK::kSfCols;                   // per stage
   extern __shared__ uint8_t smem_raw[];
@@ -375,10 +403,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + KK::kBarOff + 32 * S + 32);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = PAIR ? cluster_rank() : 0u;
-  const bool leader = rank == 0;
-  const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;    // pair or CTA index
-  const int n_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const uint32_t rank = CLU ? cluster_rank() : 0u;
+  const bool leader = !PAIR || rank == 0;                              // issues MMAs
+  const int unit = CLU ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;     // cluster or CTA index
+  const int n_units = CLU ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   const int n_blocks = (p.N + BN - 1) / BN;
   const int n_tiles = ((p.M + TM - 1) / TM) * n_blocks;
   const int num_kt = (p.K + KK::kElemsPerTile - 1) / KK::kElemsPerTile;
@@ -387,7 +415,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full + 8 * s, PAIR ? 2 : 1);   // one expect_tx arrival per producer
-      mbar_init(bar_empty + 8 * s, 1);             // the (leader's) commit
+      mbar_init(bar_empty + 8 * s, MC ? 2 : 1);    // the (leader's) commit; both CTAs' in MC
       mbar_init(bar_sfd + 8 * s, 1);
       mbar_init(bar_sf + 8 * s, PAIR ? 8 : 4);     // one arrival per scale-writer warp
     }
@@ -411,7 +439,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   }
   tc_fence_before();
-  if constexpr (PAIR) cluster_sync();
+  if constexpr (CLU) cluster_sync();
   else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
@@ -451,6 +479,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             remote_expect_tx(fb, A_BYTES + KK::kBBytes);
             tma_load_2d_pair(st, &tmA, kt * KROW, m0, fb);
             tma_load_2d_pair(st + A_BYTES, &tmB, kt * KROW, n0 + 128 * (int)rank, fb);
+          } else if constexpr (MC) {
+            // own A, own half of B into both CTAs; the peer's half lands here too
+            mbar_expect_tx(fb, A_BYTES + KK::kBBytes + sf_tx);
+            tma_load_2d(st, &tmA, kt * KROW, m0, fb);
+            tma_load_2d_mc(st + A_BYTES + (uint32_t)(128 * KROW) * rank, &tmB, kt * KROW, n0 + 128 * (int)rank, fb);
           } else {
             mbar_expect_tx(fb, A_BYTES + KK::kBBytes + sf_tx);
             tma_load_2d(st, &tmA, kt * KROW, m0, fb);
@@ -464,28 +497,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                       sf_bytes, sb);
         }
       }
+      // In a cluster the peer's commits arrive on this CTA's empty barriers:
+      // wait for the last use of every slot, so that none lands after exit.
+      if constexpr (CLU) {
+        for (int i = 0; i < S && !*abort_flag; ++i, ++it) {
+          const int s = (int)(it % S);
+          if (!mbar_wait(bar_empty + 8 * s, ((it / S) & 1u) ^ 1u, abort_flag)) {
+            *abort_flag = 1;
+            raise_status(p.status, FP4Q_DEV_TIMEOUT);
+          }
+        }
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issue (lane 0 of the leader)
+    // Nothing sits between the MMAs of a stage: a barrier test between them
+    // (measured) leaves the tensor pipe idle, as each MMA is issued only about
+    // as fast as the pipe retires one.  The next stage is waited for after
+    // the commit; at a tile's end the accumulator is committed first and the
+    // next tile's first stage is waited for once the accumulator is free.
     if (lane == 0 && leader) {
-      uint32_t it = 0, tl = 0;
+      uint32_t tl = 0, s = 0, ph = 0;
       bool ok = true;
+      // single CTA: the scale writers arrive on bar_sf only after the stage's
+      // full barrier completed, so bar_sf alone orders the operands too
+      auto stage_ready = [&](uint32_t ss, uint32_t pp) -> bool {
+        if constexpr (PAIR) return mbar_wait(bar_full + 8 * ss, pp, abort_flag) && mbar_wait(bar_sf + 8 * ss, pp, abort_flag);
+        else return mbar_wait(bar_sf + 8 * ss, pp, abort_flag);
+      };
       for (int tile = unit; tile < n_tiles && ok; tile += n_units, ++tl) {
-        ok = mbar_wait(bar_acc_empty, (tl & 1u) ^ 1u, abort_flag);
+        ok = mbar_wait(bar_acc_empty, (tl & 1u) ^ 1u, abort_flag) && stage_ready(s, ph);
         if (!ok) break;
-        tc_fence_after();
-        for (int kt = 0; kt < num_kt; ++kt, ++it) {
-          const int s = (int)(it % S);
-          const uint32_t ph = (it / S) & 1u;
-          // single CTA: the scale writers arrive on bar_sf only after the
-          // stage's full barrier completed, so bar_sf alone orders the operands too
-          if constexpr (PAIR) ok = mbar_wait(bar_full + 8 * s, ph, abort_flag) && mbar_wait(bar_sf + 8 * s, ph, abort_flag);
-          else ok = mbar_wait(bar_sf + 8 * s, ph, abort_flag);
-          if (!ok) break;
+        for (int kt = 0; kt < num_kt; ++kt) {
           tc_fence_after();
-          const uint32_t st = sbase + (uint32_t)s * KK::kStage;
-          const uint32_t sfa_col = tmem + ACC_COL + BN + SF_COLS * (uint32_t)s;
+          const uint32_t st = sbase + s * KK::kStage;
+          const uint32_t sfa_col = tmem + ACC_COL + BN + SF_COLS * s;
           const uint32_t sfb_col = sfa_col + KK::kSfColsA;
           const int rem = p.K - kt * KK::kElemsPerTile;
           const int n_mma = min(4, rem / KK::kMmaK);
@@ -506,18 +553,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             const uint32_t acc = k > 0 ? 1u : acc0;
             if constexpr (PAIR)
-              tc_mma_pair<KIND>(tmem + ACC_COL, da + 2u * k, db + 2u * k, make_idesc<KIND, TM>(sf_id), sfa, sfb, acc);
+              tc_mma_pair<KIND>(tmem + ACC_COL, da + 2u * k, db + 2u * k, make_idesc<KIND, MMA_M>(sf_id), sfa, sfb, acc);
             else
-              tc_mma<KIND>(tmem + ACC_COL, da + 2u * k, db + 2u * k, make_idesc<KIND, TM>(sf_id), sfa, sfb, acc);
+              tc_mma<KIND>(tmem + ACC_COL, da + 2u * k, db + 2u * k, make_idesc<KIND, MMA_M>(sf_id), sfa, sfb, acc);
           };
+          const bool has_next = kt + 1 < num_kt;
+          const uint32_t s2 = s + 1 == (uint32_t)S ? 0u : s + 1, ph2 = s + 1 == (uint32_t)S ? ph ^ 1u : ph;
           if (n_mma == 4) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) issue(k);
+            issue(0);
+            issue(1);
+            issue(2);
+            issue(3);
           } else {
             for (int k = 0; k < n_mma; ++k) issue(k);
           }
           if constexpr (PAIR) tc_commit_pair(bar_empty + 8 * s);
+          else if constexpr (MC) tc_commit_mc(bar_empty + 8 * s);
           else tc_commit(bar_empty + 8 * s);
+          if (has_next) ok = stage_ready(s2, ph2);
+          s = s2;
+          ph = ph2;
+          if (!ok) break;
         }
         if (!ok) break;
         if constexpr (PAIR) tc_commit_pair(bar_acc_full);
@@ -753,8 +809,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncwarp();
   }
   tc_fence_before();
-  // no CTA of a pair may leave while its peer can still use its shared or tensor memory
-  if constexpr (PAIR) cluster_sync();
+  // no CTA of a cluster may leave while its peer can still use its shared or tensor memory
+  if constexpr (CLU) cluster_sync();
   else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -777,55 +833,74 @@ bool make_out_map(CUtensorMap* m, const void* base, uint64_t N, uint64_t M, bool
                         N * (f32 ? 4u : 2u), f32 ? 32u : 64u, 32u, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int KIND, bool PAIR, int QG = -1, int QR = FP4Q_RTNE>
+template <int KIND, int CL, int QG = -1, int QR = FP4Q_RTNE>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& dh, const CUtensorMap& df,
                         const GemmParams& p, cudaStream_t s) {
-  using KK = KindK<KIND, PAIR, (QG >= 0)>;
+  constexpr bool CLU = CL != CL_SINGLE;
+  using KK = KindK<KIND, CL == CL_PAIR, (QG >= 0)>;
   static unsigned attr_set = 0;   // one bit per device ordinal < 32
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const unsigned bit = dev < 32 ? (1u << dev) : 0u;
   if (!(attr_set & bit) || !bit) {
-    e = cudaFuncSetAttribute(bs_gemm_kernel<KIND, PAIR, QG, QR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(bs_gemm_kernel<KIND, CL, QG, QR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              KK::kSmem);
     if (e != cudaSuccess) return e;
     attr_set |= bit;
   }
-  const int tm = PAIR ? 256 : BM;
+  const int tm = CLU ? 256 : BM;
   const int tiles = ((p.M + tm - 1) / tm) * ((p.N + BN - 1) / BN);
-  int units = PAIR ? num_sms() / 2 : num_sms();
-  if (tiles < units) units = tiles;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(PAIR ? 2 * units : units), 1, 1);
   cfg.blockDim = dim3(NTHREADS, 1, 1);
   cfg.dynamicSmemBytes = KK::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[0].val.clusterDim.x = CLU ? 2 : 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = PAIR ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, bs_gemm_kernel<KIND, PAIR, QG, QR>, a, b, dh, df, p);
+  cfg.numAttrs = CLU ? 1 : 0;
+  int units = num_sms();
+  if constexpr (CLU) {
+    // persistent clusters: no more than can be resident at once (a GPC with an
+    // odd number of free SMs leaves one out)
+    static int max_clusters[32] = {};
+    if (!bit || max_clusters[dev] == 0) {
+      cfg.gridDim = dim3((unsigned)num_sms() & ~1u, 1, 1);
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, bs_gemm_kernel<KIND, CL, QG, QR>, &cfg);
+      if (e != cudaSuccess) return e;
+      if (n <= 0) return cudaErrorInvalidConfiguration;
+      if (bit) max_clusters[dev] = n;
+      units = n;
+    } else {
+      units = max_clusters[dev];
+    }
+  }
+  if (tiles < units) units = tiles;
+  cfg.gridDim = dim3((unsigned)(CLU ? 2 * units : units), 1, 1);
+  return cudaLaunchKernelEx(&cfg, bs_gemm_kernel<KIND, CL, QG, QR>, a, b, dh, df, p);
 }
 
 bool al(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// The single-CTA form is the default: on the linear-layer shapes the pair form
-// measured no faster (both issue one MMA per ~190 cycles per SM, limited by
-// shared-memory traffic while TMA refills the ring) and it adds cluster-scope
-// synchronisation.  Building with -DFP4Q_GEMM_PAIR=1 selects the pair form.
-#ifndef FP4Q_GEMM_PAIR
-#define FP4Q_GEMM_PAIR 0
+// Cooperation form of the plain GEMM kernels, -DFP4Q_GEMM_CLUSTER=0/1/2:
+// single CTA, cta_group::2 pair, multicast cluster.  The fused-quantization
+// kernels use the single or multicast form (the pair form is not built for them).
+#ifndef FP4Q_GEMM_CLUSTER
+#define FP4Q_GEMM_CLUSTER 0
 #endif
-constexpr bool kPair = FP4Q_GEMM_PAIR != 0;
+constexpr int kCluster = FP4Q_GEMM_CLUSTER;
+static_assert(kCluster == CL_SINGLE || kCluster == CL_PAIR || kCluster == CL_MC, "FP4Q_GEMM_CLUSTER");
+template <int QG>
+constexpr int cluster_form() { return (kCluster == CL_PAIR && QG >= 0) ? CL_SINGLE : kCluster; }
 
 // Checks shared by the two entry points, the kernel parameters and the
 // operand / output tensor maps.  Returns FP4Q_OK or the error status.
 int32_t prepare_gemm(const fp4q_operand* A, const fp4q_operand* B, int64_t M, int64_t N, int64_t K, int32_t grid,
-                     int32_t scale, void* D_bf16, float* D_f32, uint32_t* d_status, int& kind, GemmParams& p,
+                     int32_t scale, void* D_bf16, float* D_f32, uint32_t* d_status, int cl, int& kind, GemmParams& p,
                      CUtensorMap& ta, CUtensorMap& tb, CUtensorMap& tdh, CUtensorMap& tdf) {
   if (!A || !B) return FP4Q_ERR_INVALID_ARG;
   if (grid != FP4Q_GRID_E2M1 && grid != FP4Q_GRID_E1M2 && grid != FP4Q_GRID_E2M1_R4) return FP4Q_ERR_INVALID_ARG;
@@ -857,7 +932,7 @@ int32_t prepare_gemm(const fp4q_operand* A, const fp4q_operand* B, int64_t M, in
   memset(&tdh, 0, sizeof(tdh));
   memset(&tdf, 0, sizeof(tdf));
   if (!make_map(&ta, a_data, row_bytes, (uint64_t)M, BM) ||
-      !make_map(&tb, b_data, row_bytes, (uint64_t)N, KindK<KIND_MXF4, kPair>::kBRows))
+      !make_map(&tb, b_data, row_bytes, (uint64_t)N, cl == CL_SINGLE ? 256u : 128u))
     return FP4Q_ERR_CUDA;
   if (D_bf16 && !make_out_map(&tdh, D_bf16, (uint64_t)N, (uint64_t)M, false)) return FP4Q_ERR_CUDA;
   if (D_f32 && !make_out_map(&tdf, D_f32, (uint64_t)N, (uint64_t)M, true)) return FP4Q_ERR_CUDA;
@@ -867,9 +942,10 @@ int32_t prepare_gemm(const fp4q_operand* A, const fp4q_operand* B, int64_t M, in
 template <int QG, int QR>
 cudaError_t launch_kind(int kind, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tdh,
                         const CUtensorMap& tdf, const GemmParams& p, cudaStream_t s) {
-  if (kind == KIND_MXF4) return launch_gemm<KIND_MXF4, kPair && QG < 0, QG, QR>(ta, tb, tdh, tdf, p, s);
-  if (kind == KIND_NVF4) return launch_gemm<KIND_NVF4, kPair && QG < 0, QG, QR>(ta, tb, tdh, tdf, p, s);
-  return launch_gemm<KIND_F8, kPair && QG < 0, QG, QR>(ta, tb, tdh, tdf, p, s);
+  constexpr int cl = cluster_form<QG>();
+  if (kind == KIND_MXF4) return launch_gemm<KIND_MXF4, cl, QG, QR>(ta, tb, tdh, tdf, p, s);
+  if (kind == KIND_NVF4) return launch_gemm<KIND_NVF4, cl, QG, QR>(ta, tb, tdh, tdf, p, s);
+  return launch_gemm<KIND_F8, cl, QG, QR>(ta, tb, tdh, tdf, p, s);
 }
 
 }  // namespace
@@ -883,7 +959,8 @@ extern "C" int32_t fp4q_gemm(const fp4q_operand* A, const fp4q_operand* B, int64
   int kind = 0;
   GemmParams p;
   CUtensorMap ta, tb, tdh, tdf;
-  const int32_t st = prepare_gemm(A, B, M, N, K, grid, scale, D_bf16, D_f32, d_status, kind, p, ta, tb, tdh, tdf);
+  const int32_t st = prepare_gemm(A, B, M, N, K, grid, scale, D_bf16, D_f32, d_status, cluster_form<-1>(), kind, p,
+                                  ta, tb, tdh, tdf);
   if (st != FP4Q_OK) return st;
   const cudaError_t e = launch_kind<-1, FP4Q_RTNE>(kind, ta, tb, tdh, tdf, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
@@ -907,7 +984,8 @@ extern "C" int32_t fp4q_gemm_quantize(const fp4q_operand* A, const fp4q_operand*
   int kind = 0;
   GemmParams p;
   CUtensorMap ta, tb, tdh, tdf;
-  const int32_t st = prepare_gemm(A, B, M, N, K, grid, scale, D_bf16, nullptr, d_status, kind, p, ta, tb, tdh, tdf);
+  const int32_t st = prepare_gemm(A, B, M, N, K, grid, scale, D_bf16, nullptr, d_status, cluster_form<0>(), kind, p,
+                                  ta, tb, tdh, tdf);
   if (st != FP4Q_OK) return st;
   p.q_codes = out->codes;
   p.q_scales = out->scales;
