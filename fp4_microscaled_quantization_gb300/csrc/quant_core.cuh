@@ -59,38 +59,60 @@ __device__ __forceinline__ uint32_t rtne_e1m2(float v) {
   return (__float_as_uint(t) & 7u) | ((__float_as_uint(v) >> 28) & 8u);
 }
 
-// Exact stochastic-rounding decision shared by both grids.  With s >= 0 the
-// position on a unit-spaced grid (s < 8), t = fl_rm(s + 2^23) holds floor(s) in
-// its low bits; C = 2^23 - floor(s) 2^16 is exact; y = fl_ru(s 2^16 + C) =
-// 2^23 + ceil(frac(s) 2^16); and r16 < frac(s) 2^16 (the rule r / 2^16 < f)
-// holds iff 2^23 + r16 < y.  Returns floor(s) + up.
-__device__ __forceinline__ uint32_t sr_unit(float s, float r_as_float) {
-  float t, y;
-  asm("add.rm.f32 %0, %1, %2;" : "=f"(t) : "f"(s), "f"(8388608.0f));
-  const float C = __fmaf_rn(t, -65536.0f, 549764202496.0f);   // 2^39 + 2^23 - t 2^16
-  asm("fma.rp.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(s), "f"(65536.0f), "f"(C));
-  return (__float_as_uint(t) & 7u) + ((r_as_float < y) ? 1u : 0u);
-}
-
 // 2^23 + r as a float, r the 16-bit uniform numerator (exact).
 __device__ __forceinline__ float r16_float(uint32_t r16) { return __uint_as_float(0x4B000000u | r16); }
 
-// SR onto {k/4}: s = 4 min(|v|, 1.75) is exact and lies on the unit grid.
-__device__ __forceinline__ uint32_t sr_e1m2(float v, float rf) {
-  const float s = fminf(fabsf(v), 1.75f) * 4.0f;
-  return sr_unit(s, rf) | ((__float_as_uint(v) >> 28) & 8u);
+// Stochastic rounding, two elements at a time: the fp32 steps are packed
+// f32x2 instructions, each lane rounded as the scalar instruction would be.
+__device__ __forceinline__ uint64_t pack2(float2 a) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+  return r;
 }
-
+__device__ __forceinline__ float2 unpack2(uint64_t d) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+  return r;
+}
+// Exact decision shared by all grids.  With s >= 0 the position on a
+// unit-spaced grid (s < 8), t = fl_rm(s + 2^23) holds floor(s) in its low
+// bits; C = 2^39 + 2^23 - t 2^16 = 2^23 - floor(s) 2^16 is exact; y =
+// fl_ru(s 2^16 + C) = 2^23 + ceil(frac(s) 2^16); and r16 < frac(s) 2^16 (the
+// rule r / 2^16 < f) holds iff 2^23 + r16 < y.  Returns floor(s) + up; rf is
+// r16_float of the element's random numerator.
+__device__ __forceinline__ uint2 sr_unit2(float2 s, float2 rf) {
+  uint64_t t, c, y;
+  const uint64_t ss = pack2(s);
+  asm("add.rm.f32x2 %0, %1, %2;" : "=l"(t) : "l"(ss), "l"(pack2(make_float2(8388608.0f, 8388608.0f))));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(c)
+      : "l"(t), "l"(pack2(make_float2(-65536.0f, -65536.0f))),
+        "l"(pack2(make_float2(549764202496.0f, 549764202496.0f))));
+  asm("fma.rp.f32x2 %0, %1, %2, %3;" : "=l"(y) : "l"(ss), "l"(pack2(make_float2(65536.0f, 65536.0f))), "l"(c));
+  const float2 tt = unpack2(t), yy = unpack2(y);
+  return make_uint2((__float_as_uint(tt.x) & 7u) + ((rf.x < yy.x) ? 1u : 0u),
+                    (__float_as_uint(tt.y) & 7u) + ((rf.y < yy.y) ? 1u : 0u));
+}
+// SR onto {k/4}: s = 4 min(|v|, 1.75) is exact and lies on the unit grid.
+__device__ __forceinline__ uint2 sr_e1m2_2(float2 v, float2 rf) {
+  const float2 s = mul2(make_float2(fminf(fabsf(v.x), 1.75f), fminf(fabsf(v.y), 1.75f)), make_float2(4.0f, 4.0f));
+  const uint2 u = sr_unit2(s, rf);
+  return make_uint2(u.x | ((__float_as_uint(v.x) >> 28) & 8u), u.y | ((__float_as_uint(v.y) >> 28) & 8u));
+}
 // SR onto E2M1: with E = clamp(floor(log2 |v|), 0, 2) the levels around |v|
-// are 2^(E-1) apart, s = |v| 2^(1-E) is exact, and the lower level's code is
+// are 2^(E-1) apart, s = |v| 2^(1-E) is exact (2^(1-E) has exponent field
+// 0x7F800000 - eb, eb = (127 + E) << 23), and the lower level's code is
 // 2E + floor(s) (floor(s) = 0..3 for E = 0, 2..3 above).
 template <int CAP = 6>
-__device__ __forceinline__ uint32_t sr_e2m1(float v, float rf) {
-  const float a = fminf(fabsf(v), (float)CAP);
-  const uint32_t eb = __float_as_uint(fmaxf(a, 1.0f)) & 0x7F800000u;   // (127 + E) << 23
-  const float s = a * __uint_as_float(0x7F800000u - eb);              // 2^(1-E), exponent 128 - E
-  const uint32_t twoE = (eb >> 22) - 254u;
-  return (twoE + sr_unit(s, rf)) | ((__float_as_uint(v) >> 28) & 8u);
+__device__ __forceinline__ uint2 sr_e2m1_2(float2 v, float2 rf) {
+  const float ax = fminf(fabsf(v.x), (float)CAP), ay = fminf(fabsf(v.y), (float)CAP);
+  const uint32_t ebx = __float_as_uint(fmaxf(ax, 1.0f)) & 0x7F800000u;
+  const uint32_t eby = __float_as_uint(fmaxf(ay, 1.0f)) & 0x7F800000u;
+  const float2 s = mul2(make_float2(ax, ay),
+                        make_float2(__uint_as_float(0x7F800000u - ebx), __uint_as_float(0x7F800000u - eby)));
+  const uint2 u = sr_unit2(s, rf);
+  return make_uint2((((ebx >> 22) - 254u) + u.x) | ((__float_as_uint(v.x) >> 28) & 8u),
+                    (((eby >> 22) - 254u) + u.y) | ((__float_as_uint(v.y) >> 28) & 8u));
 }
 
 // E4M3 bytes of eight packed codes (element 0 in the low nibble): magnitude by
@@ -231,22 +253,28 @@ __device__ __forceinline__ void quantize_chunk(float2 (&P)[16], float S_t, uint6
   } else {
     // stochastic rounding: element t of the chunk takes half (t & 1) of word
     // (t >> 1) & 3 of Philox call t >> 3, counter (idx >> 3) of the copy.
+    // Elements 8h + j (P[8h + j].x, output word h) and 16 + 8h + j (its .y,
+    // word h + 2) take the same half of the same word of calls h and h + 2,
+    // and are decided together.
     const uint64_t c = idx0 >> 3;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint64_t cq = c + (uint64_t)q;
-      const Philox4 r = philox4x32_10((uint32_t)cq, (uint32_t)(cq >> 32), orient, 0u, key0, key1);
-      uint32_t w = 0;
+    for (int h = 0; h < 2; ++h) {
+      const uint64_t ca = c + (uint64_t)h, cb = ca + 2u;
+      const Philox4 ra = philox4x32_10((uint32_t)ca, (uint32_t)(ca >> 32), orient, 0u, key0, key1);
+      const Philox4 rb = philox4x32_10((uint32_t)cb, (uint32_t)(cb >> 32), orient, 0u, key0, key1);
+      uint32_t wa = 0, wb = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const int t = q * 8 + j;
-        const float v = (t < 16) ? P[t].x : P[t - 16].y;
-        const float rf = r16_float((j & 1) ? (r.v[j >> 1] >> 16) : (r.v[j >> 1] & 0xFFFFu));
-        const uint32_t code = (GRID == FP4Q_GRID_E1M2) ? sr_e1m2(v, rf)
-                              : (GRID == FP4Q_GRID_E2M1_R4) ? sr_e2m1<4>(v, rf) : sr_e2m1<6>(v, rf);
-        w |= code << (4 * j);
+        const float2 rf = (j & 1) ? make_float2(r16_float(ra.v[j >> 1] >> 16), r16_float(rb.v[j >> 1] >> 16))
+                                  : make_float2(r16_float(ra.v[j >> 1] & 0xFFFFu), r16_float(rb.v[j >> 1] & 0xFFFFu));
+        const uint2 code = (GRID == FP4Q_GRID_E1M2) ? sr_e1m2_2(P[8 * h + j], rf)
+                           : (GRID == FP4Q_GRID_E2M1_R4) ? sr_e2m1_2<4>(P[8 * h + j], rf)
+                                                         : sr_e2m1_2<6>(P[8 * h + j], rf);
+        wa |= code.x << (4 * j);
+        wb |= code.y << (4 * j);
       }
-      o.w[q] = w;
+      o.w[h] = wa;
+      o.w[h + 2] = wb;
     }
   }
   if (emit_e4m3) {
