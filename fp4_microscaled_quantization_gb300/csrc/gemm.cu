@@ -9,8 +9,9 @@
 //   E1M2 + MX                    -> kind::mxf8f6f4 on the E4M3 byte copies
 //                                   (every E1M2 level k/4 is exact in E4M3)
 //
-// Structure (persistent, 320 threads per CTA; a single CTA per 128 x 256
-// output tile, or a pair of CTAs per 256 x 256 tile, see the kernel):
+// Structure (persistent, 448 threads per CTA, 320 for the kernels that
+// quantize their output; a single CTA per 128 x 256 output tile, or two CTAs
+// per 256 x 256 tile, see the kernel):
 //   warp 0      TMA producer: A/B tiles (128-byte swizzled K-major rows) by
 //               cp.async.bulk.tensor and the compact 512-byte scale chunks by
 //               cp.async.bulk, into a ring of stages guarded by mbarriers.
@@ -18,10 +19,12 @@
 //               once its operands and scales are in place, and tcgen05.commit
 //               frees the stage.
 //   warps 2-5   epilogue: TMEM -> registers (tcgen05.ld), alpha, bf16/fp32,
-//               then a swizzled shared-memory box stored by TMA
+//   (+ 10-13)   then a swizzled shared-memory box stored by TMA
 //               (cp.async.bulk.tensor, bulk groups).  The accumulator is
 //               released before the stores so the next tile's MMAs overlap
-//               them.
+//               them.  The plain kernels drain it with eight warps, two per
+//               TMEM lane quarter (columns 0-127 and 128-255), which halves
+//               the time the next tile's MMAs wait for it.
 //   warps 6-9   scale writers, one per TMEM lane quarter: per stage they read
 //               the compact chunks from shared memory and write them to TMEM
 //               with tcgen05.st, then signal the MMA lane.
@@ -63,10 +66,8 @@ constexpr int BM = 128;              // accumulator rows per CTA (TMEM lanes)
 constexpr int BN = 256;              // tile columns (MMA N)
 constexpr int KROW = 128;            // bytes of one operand row per K-tile (one 128B swizzle span)
 constexpr int A_BYTES = BM * KROW;   // 16 KB
-constexpr int NTHREADS = 320;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;      // accumulator columns [0, 256); scale columns after it
-constexpr int STG_BYTES = 4096;      // one epilogue store box (32 rows x 128 bytes)
 
 template <int KIND, bool PAIR, bool FUSED = false>
 struct KindK {
@@ -87,14 +88,18 @@ struct KindK {
   // (two for NV) 32x32b.x32 store, or one x16 for F8
   static constexpr int kSfCols = KIND == KIND_MXF4 ? 32 : (KIND == KIND_NVF4 ? 64 : 16);
   static constexpr int kStage = (A_BYTES + kBBytes + kCompact + 1023) / 1024 * 1024;
-  // epilogue staging per warp: one 32 x 64 bf16 store box, or (fused output
-  // quantization) the warp's whole 32 x 256 bf16 slice of the tile
-  static constexpr int kStgWarp = FUSED ? 4 * STG_BYTES : STG_BYTES;
-  static constexpr int kStagesMax = (232448 - 1280 - 4 * kStgWarp) / kStage;
+  // threads: producer, MMA, scale-writer warps and the epilogue warps (4,
+  // or 8 when two drain each TMEM lane quarter)
+  static constexpr int kEpiWarps = FUSED ? 4 : 8;
+  static constexpr int kThreads = 32 * (6 + kEpiWarps);
+  // epilogue staging per warp: one 32-row x 64-byte store box, or (fused
+  // output quantization) the warp's whole 32 x 256 bf16 slice of the tile
+  static constexpr int kStgWarp = FUSED ? 16384 : 2048;
+  static constexpr int kStagesMax = (232448 - 1280 - kEpiWarps * kStgWarp) / kStage;
   static constexpr int kStagesCap = kStagesMax > 6 ? 6 : kStagesMax;
   static constexpr int kStagesTmem = (int)(TMEM_COLS - BN) / kSfCols;   // stages whose scales fit beside the accumulator
   static constexpr int kStages = kStagesCap > kStagesTmem ? kStagesTmem : kStagesCap;
-  static constexpr int kBarOff = kStages * kStage + 4 * kStgWarp;    // stages, then the epilogue staging
+  static constexpr int kBarOff = kStages * kStage + kEpiWarps * kStgWarp;   // stages, then the epilogue staging
   static constexpr int kSmem = kBarOff + 256 + 1024;                 // + barriers + alignment slack
   static_assert(kStages >= (FUSED ? 2 : 3), "pipeline depth");
   static_assert(kSmem <= 232448, "shared memory");
@@ -377,7 +382,7 @@ __device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, 
 // every commit arrives on the empty barrier of both CTAs.
 // Tile id -> (m block = id / n_blocks, n block = id % n_blocks).
 template <int KIND, int CL, int QG = -1, int QR = FP4Q_RTNE>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThreads, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmDh, const __grid_constant__ CUtensorMap tmDf,
                    const GemmParams p) {
@@ -420,7 +425,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(bar_sf + 8 * s, PAIR ? 8 : 4);     // one arrival per scale-writer warp
     }
     mbar_init(bar_acc_full, 1);
-    mbar_init(bar_acc_empty, PAIR ? 8 : 4);        // one arrival per epilogue warp
+    mbar_init(bar_acc_empty, (PAIR ? 2 : 1) * KK::kEpiWarps);   // one arrival per epilogue warp
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -594,7 +599,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp >= 6) {
+  } else if (warp >= 6 && warp < 10) {
     // ---------------- scale writers: lane i of quarter q stores row i of the compact chunks
     const uint32_t qbase = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     uint32_t it = 0;
@@ -643,13 +648,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       raise_status(p.status, FP4Q_DEV_TIMEOUT);
     }
   } else {
-    // ---------------- epilogue (warps 2..5 -> TMEM lane quarters 2, 3, 0, 1)
+    // ---------------- epilogue (warps 2..5 and 10..13 -> TMEM lane quarters 2, 3, 0, 1)
     const int sp = warp & 3;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * sp) << 16) + ACC_COL;
-    const uint32_t stg = stg_base + (uint32_t)(warp - 2) * KK::kStgWarp;
-    // 128B-swizzled box row `lane`: 16-byte unit u of the row sits at unit u ^ (lane & 7)
-    const uint32_t row_off = 128u * (uint32_t)lane;
-    const uint32_t swz = (uint32_t)(lane & 7);
+    const int epi = warp < 6 ? warp - 2 : warp - 6;                 // 0..7
+    const uint32_t stg = stg_base + (uint32_t)epi * KK::kStgWarp;
+    // fused kernels: 128B-swizzled 32 x 64 bf16 boxes, 16-byte unit u of row
+    // `lane` at unit u ^ (lane & 7); plain kernels: 64B-swizzled 32-row x
+    // 64-byte boxes, unit u of row `lane` at unit u ^ ((lane >> 1) & 3)
+    const uint32_t row_off = (QG >= 0 ? 128u : 64u) * (uint32_t)lane;
+    const uint32_t swz = QG >= 0 ? (uint32_t)(lane & 7) : (uint32_t)((lane >> 1) & 3);
+    const int cbase = warp >= 10 ? 128 : 0;                         // this warp's accumulator columns
     float alpha = 1.0f;
     if constexpr (KIND == KIND_NVF4) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
     uint32_t tl = 0;
@@ -744,29 +753,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         continue;
       }
-      uint32_t h[BN / 2];                    // the row as packed bf16
+      uint32_t h[64];   // this warp's 128 columns of the row as packed bf16
 #pragma unroll
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        if (c0 < ncols) {
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        if (cbase + c0 < ncols) {
           uint32_t r[32];
-          tmem_ld32(lane_base + (uint32_t)c0, r);
+          tmem_ld32(lane_base + (uint32_t)(cbase + c0), r);
           if constexpr (KIND == KIND_NVF4) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), alpha));
           }
           if (p.want_f32 && live) {
-            // one 32-row x 32-float box per 32 columns
-            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-            __syncwarp();
+            // two 32-row x 16-float boxes per 32 columns
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              st_shared16(stg + row_off + 16u * ((uint32_t)u ^ swz),
-                          make_uint4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]));
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tmDf, n0 + c0, y, stg);
-              asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            for (int hh = 0; hh < 2; ++hh) {
+              if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+              __syncwarp();
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                st_shared16(stg + row_off + 16u * ((uint32_t)u ^ swz),
+                            make_uint4(r[16 * hh + 4 * u], r[16 * hh + 4 * u + 1], r[16 * hh + 4 * u + 2],
+                                       r[16 * hh + 4 * u + 3]));
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmDf, n0 + cbase + c0 + 16 * hh, y, stg);
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+              }
             }
           }
 #pragma unroll
@@ -784,21 +797,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         else mbar_arrive(lead_acc_empty);
       }
       if (p.want_bf16 && live) {
-        // one 32-row x 64-bf16 box per 64 columns
+        // one 32-row x 32-bf16 box per 32 columns
 #pragma unroll
-        for (int b = 0; b < BN / 64; ++b) {
-          if (64 * b < ncols) {
+        for (int b = 0; b < 4; ++b) {
+          if (cbase + 32 * b < ncols) {
             if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             __syncwarp();
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
+            for (int u = 0; u < 4; ++u)
               st_shared16(stg + row_off + 16u * ((uint32_t)u ^ swz),
-                          make_uint4(h[32 * b + 4 * u], h[32 * b + 4 * u + 1], h[32 * b + 4 * u + 2],
-                                     h[32 * b + 4 * u + 3]));
+                          make_uint4(h[16 * b + 4 * u], h[16 * b + 4 * u + 1], h[16 * b + 4 * u + 2],
+                                     h[16 * b + 4 * u + 3]));
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tmDh, n0 + 64 * b, y, stg);
+              tma_store_2d(&tmDh, n0 + cbase + 32 * b, y, stg);
               asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             }
           }
@@ -827,10 +840,12 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t row
   return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, (uint32_t)KROW,
                         box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
-// Output [M][N] of bf16 (box 64 x 32) or fp32 (box 32 x 32), 128B swizzle.
-bool make_out_map(CUtensorMap* m, const void* base, uint64_t N, uint64_t M, bool f32) {
+// Output [M][N] of bf16 or fp32, boxes of 32 rows x box_bytes (64 with 64B
+// swizzle for the plain kernels, 128 with 128B swizzle for the fused ones).
+bool make_out_map(CUtensorMap* m, const void* base, uint64_t N, uint64_t M, bool f32, uint32_t box_bytes) {
   return encode_tmap_2d(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, N, M,
-                        N * (f32 ? 4u : 2u), f32 ? 32u : 64u, 32u, CU_TENSOR_MAP_SWIZZLE_128B);
+                        N * (f32 ? 4u : 2u), box_bytes / (f32 ? 4u : 2u), 32u,
+                        box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int KIND, int CL, int QG = -1, int QR = FP4Q_RTNE>
@@ -852,7 +867,7 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtens
   const int tm = CLU ? 256 : BM;
   const int tiles = ((p.M + tm - 1) / tm) * ((p.N + BN - 1) / BN);
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(NTHREADS, 1, 1);
+  cfg.blockDim = dim3(KK::kThreads, 1, 1);
   cfg.dynamicSmemBytes = KK::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -900,8 +915,8 @@ constexpr int cluster_form() { return (kCluster == CL_PAIR && QG >= 0) ? CL_SING
 // Checks shared by the two entry points, the kernel parameters and the
 // operand / output tensor maps.  Returns FP4Q_OK or the error status.
 int32_t prepare_gemm(const fp4q_operand* A, const fp4q_operand* B, int64_t M, int64_t N, int64_t K, int32_t grid,
-                     int32_t scale, void* D_bf16, float* D_f32, uint32_t* d_status, int cl, int& kind, GemmParams& p,
-                     CUtensorMap& ta, CUtensorMap& tb, CUtensorMap& tdh, CUtensorMap& tdf) {
+                     int32_t scale, void* D_bf16, float* D_f32, uint32_t* d_status, int cl, bool fused, int& kind,
+                     GemmParams& p, CUtensorMap& ta, CUtensorMap& tb, CUtensorMap& tdh, CUtensorMap& tdf) {
   if (!A || !B) return FP4Q_ERR_INVALID_ARG;
   if (grid != FP4Q_GRID_E2M1 && grid != FP4Q_GRID_E1M2 && grid != FP4Q_GRID_E2M1_R4) return FP4Q_ERR_INVALID_ARG;
   if (scale != FP4Q_SCALE_MX && scale != FP4Q_SCALE_NV) return FP4Q_ERR_INVALID_ARG;
@@ -934,8 +949,8 @@ int32_t prepare_gemm(const fp4q_operand* A, const fp4q_operand* B, int64_t M, in
   if (!make_map(&ta, a_data, row_bytes, (uint64_t)M, BM) ||
       !make_map(&tb, b_data, row_bytes, (uint64_t)N, cl == CL_SINGLE ? 256u : 128u))
     return FP4Q_ERR_CUDA;
-  if (D_bf16 && !make_out_map(&tdh, D_bf16, (uint64_t)N, (uint64_t)M, false)) return FP4Q_ERR_CUDA;
-  if (D_f32 && !make_out_map(&tdf, D_f32, (uint64_t)N, (uint64_t)M, true)) return FP4Q_ERR_CUDA;
+  if (D_bf16 && !make_out_map(&tdh, D_bf16, (uint64_t)N, (uint64_t)M, false, fused ? 128u : 64u)) return FP4Q_ERR_CUDA;
+  if (D_f32 && !make_out_map(&tdf, D_f32, (uint64_t)N, (uint64_t)M, true, 64u)) return FP4Q_ERR_CUDA;
   return FP4Q_OK;
 }
 
@@ -959,8 +974,8 @@ extern "C" int32_t fp4q_gemm(const fp4q_operand* A, const fp4q_operand* B, int64
   int kind = 0;
   GemmParams p;
   CUtensorMap ta, tb, tdh, tdf;
-  const int32_t st = prepare_gemm(A, B, M, N, K, grid, scale, D_bf16, D_f32, d_status, cluster_form<-1>(), kind, p,
-                                  ta, tb, tdh, tdf);
+  const int32_t st = prepare_gemm(A, B, M, N, K, grid, scale, D_bf16, D_f32, d_status, cluster_form<-1>(), false,
+                                  kind, p, ta, tb, tdh, tdf);
   if (st != FP4Q_OK) return st;
   const cudaError_t e = launch_kind<-1, FP4Q_RTNE>(kind, ta, tb, tdh, tdf, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
@@ -984,8 +999,8 @@ extern "C" int32_t fp4q_gemm_quantize(const fp4q_operand* A, const fp4q_operand*
   int kind = 0;
   GemmParams p;
   CUtensorMap ta, tb, tdh, tdf;
-  const int32_t st = prepare_gemm(A, B, M, N, K, grid, scale, D_bf16, nullptr, d_status, cluster_form<0>(), kind, p,
-                                  ta, tb, tdh, tdf);
+  const int32_t st = prepare_gemm(A, B, M, N, K, grid, scale, D_bf16, nullptr, d_status, cluster_form<0>(), true,
+                                  kind, p, ta, tb, tdh, tdf);
   if (st != FP4Q_OK) return st;
   p.q_codes = out->codes;
   p.q_scales = out->scales;
