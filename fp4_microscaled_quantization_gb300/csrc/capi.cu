@@ -72,6 +72,7 @@ int32_t prepare(const void* x, int64_t rows, int64_t cols, int64_t ld, const fp4
   p.cols = cols;
   p.ld = ld;
   p.sr_seed = cfg->sr_seed;
+  philox_round_keys(cfg->sr_seed, p.sr_keys);
   p.want_row = cfg->want_row ? 1 : 0;
   p.want_col = cfg->want_col ? 1 : 0;
   p.sf_mma = cfg->sf_layout == FP4Q_SF_MMA ? 1 : 0;

@@ -25,6 +25,7 @@ struct QuantParams {
   const float* gamax;  // NV: G of the (row, col) copies
   uint32_t* status;
   uint64_t sr_seed;
+  uint32_t sr_keys[20];  // Philox round keys of sr_seed (philox_round_keys)
   int32_t want_row, want_col, sf_mma, emit_e4m3;
   uint32_t sgn_row[32];  // bit 31 set: negate element t of a 32-element chunk (row-wise)
   uint32_t sgn_col[32];  // same, column-wise copy

@@ -121,6 +121,7 @@ struct GemmParams {
   uint8_t* q_scales;      // M x N/32 E8M0 bytes, plain or MMA layout
   uint8_t* q_e4m3;        // optional M x N E4M3 bytes
   uint64_t q_seed;        // stochastic rounding
+  uint32_t q_keys[20];    // its Philox round keys
   int32_t q_nh, q_sf_mma;
   uint32_t q_sgn[32];     // sign words of a 32-element chunk (bit 31 = negate)
 };
@@ -739,8 +740,8 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
             else if (p.q_nh == 32) rotate_chunk<32>(P);
             ChunkOut o;
             const int64_t col = (int64_t)n0 + c0;
-            quantize_chunk<QG, FP4Q_SCALE_MX, QR>(P, 0.0f, (uint64_t)(row * p.N + col), 0u, (uint32_t)p.q_seed,
-                                                  (uint32_t)(p.q_seed >> 32), p.q_e4m3 != nullptr, p.status, o);
+            quantize_chunk<QG, FP4Q_SCALE_MX, QR>(P, 0.0f, (uint64_t)(row * p.N + col), 0u, p.q_keys,
+                                                  p.q_e4m3 != nullptr, p.status, o);
             *reinterpret_cast<uint4*>(p.q_codes + row * (p.N / 2) + col / 2) = make_uint4(o.w[0], o.w[1], o.w[2], o.w[3]);
             const int64_t nkb = p.N / 32, k = col / 32;
             p.q_scales[p.q_sf_mma ? sf_mma_offset(row, k, nkb) : row * nkb + k] = (uint8_t)o.sbytes;
@@ -1006,6 +1007,7 @@ extern "C" int32_t fp4q_gemm_quantize(const fp4q_operand* A, const fp4q_operand*
   p.q_scales = out->scales;
   p.q_e4m3 = c.emit_e4m3 ? out->e4m3 : nullptr;
   p.q_seed = c.sr_seed;
+  philox_round_keys(c.sr_seed, p.q_keys);
   p.q_nh = c.rot;
   p.q_sf_mma = c.sf_layout == FP4Q_SF_MMA;
   for (int t = 0; t < 32; ++t) p.q_sgn[t] = (c.rot && ((c.sign_mask_row >> (t % c.rot)) & 1u)) ? 0x80000000u : 0u;

@@ -247,7 +247,6 @@ constexpr int quant_ctas() { return ROUND == FP4Q_SR ? 2 : QUANT_MIN_CTAS; }
 template <int GRID, int SCALE, int NH, int ROUND>
 __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
     rht_quant_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
-  const uint32_t key0 = (uint32_t)p.sr_seed, key1 = (uint32_t)(p.sr_seed >> 32);
   constexpr float kDen = 448.0f * GridK<GRID>::kQmax;
   float S_row = 0.0f, S_col = 0.0f;
   if constexpr (SCALE == FP4Q_SCALE_NV) {
@@ -272,7 +271,7 @@ __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
         read_col_chunk(tv, threadIdx.x, p.sgn_col, P);
         rotate_chunk<NH>(P);
         ChunkOut o;
-        quantize_chunk<GRID, SCALE, ROUND>(P, S_col, (uint64_t)(c * p.rows + tr0), 1u, key0, key1,
+        quantize_chunk<GRID, SCALE, ROUND>(P, S_col, (uint64_t)(c * p.rows + tr0), 1u, p.sr_keys,
                                            p.emit_e4m3, p.status, o);
         store_chunk<SCALE>(p.col, c, tr0, p.rows, p.sf_mma, p.emit_e4m3, o);
       }
@@ -286,7 +285,7 @@ __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
         read_row_chunk(tv, r, q, p.sgn_row, P);
         rotate_chunk<NH>(P);
         ChunkOut o;
-        quantize_chunk<GRID, SCALE, ROUND>(P, S_row, (uint64_t)(gr * p.cols + gc), 0u, key0, key1,
+        quantize_chunk<GRID, SCALE, ROUND>(P, S_row, (uint64_t)(gr * p.cols + gc), 0u, p.sr_keys,
                                            p.emit_e4m3, p.status, o);
         store_chunk<SCALE>(p.row, gr, gc, p.cols, p.sf_mma, p.emit_e4m3, o);
       }

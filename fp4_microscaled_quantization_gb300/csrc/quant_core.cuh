@@ -183,7 +183,7 @@ struct ChunkOut {
 //   idx0   index of element 0 in the stored copy (multiple of 32), for SR
 template <int GRID, int SCALE, int ROUND>
 __device__ __forceinline__ void quantize_chunk(float2 (&P)[16], float S_t, uint64_t idx0,
-                                               uint32_t orient, uint32_t key0, uint32_t key1,
+                                               uint32_t orient, const uint32_t (&rk)[20],
                                                bool emit_e4m3, uint32_t* status, ChunkOut& o) {
   constexpr float QMAX = GridK<GRID>::kQmax;
   // block amax (NaN-propagating)
@@ -260,8 +260,8 @@ __device__ __forceinline__ void quantize_chunk(float2 (&P)[16], float S_t, uint6
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint64_t ca = c + (uint64_t)h, cb = ca + 2u;
-      const Philox4 ra = philox4x32_10((uint32_t)ca, (uint32_t)(ca >> 32), orient, 0u, key0, key1);
-      const Philox4 rb = philox4x32_10((uint32_t)cb, (uint32_t)(cb >> 32), orient, 0u, key0, key1);
+      const Philox4 ra = philox4x32_10_rk((uint32_t)ca, (uint32_t)(ca >> 32), orient, 0u, rk);
+      const Philox4 rb = philox4x32_10_rk((uint32_t)cb, (uint32_t)(cb >> 32), orient, 0u, rk);
       uint32_t wa = 0, wb = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
