@@ -250,9 +250,12 @@ def run_ours(args, world, rank, local):
     hY, hdX, hdW = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (Y, dX, dW))
     h2d = sum(t.numel() * t.element_size() for t in (hX, hW, hdY))
     d2h = sum(t.numel() * t.element_size() for t in (hY, hdX, hdW))
-    # host<->device copies run on a copy stream: the uploads of W and dY overlap
-    # the quantization of X, and the download of each GEMM's output overlaps
-    # the GEMMs after it; every compute step waits for its own input's upload
+    # host<->device copies run on a copy stream (one copy engine's worth of link
+    # bandwidth: splitting a copy over more streams measured no faster).  The
+    # uploads go in the order dY, X, W so that the longest quantization (dY,
+    # stochastic rounding) overlaps the uploads after it and only W's short one
+    # is left at the end; the download of each GEMM's output overlaps the GEMMs
+    # after it; every compute step waits for its own input's upload
     copy_stream = torch.cuda.Stream(dev)
     e2e_q, e2e_g = [], []
     for it in range(args.warmup + args.steps):
@@ -262,10 +265,10 @@ def run_ours(args, world, rank, local):
         copy_stream.wait_event(e0)
         up = [ev() for _ in range(3)]
         with torch.cuda.stream(copy_stream):
-            for dst, src, u in ((X, hX, up[0]), (W, hW, up[1]), (dY, hdY, up[2])):
+            for dst, src, u in ((dY, hdY, up[0]), (X, hX, up[1]), (W, hW, up[2])):
                 dst.copy_(src, non_blocking=True)
                 u.record(copy_stream)
-        for u, (x, cfg, ro, co) in zip(up, ((X, cfg_x, Xr, Xc), (W, cfg_w, Wr, Wc), (dY, cfg_g, Gr, Gc))):
+        for u, (x, cfg, ro, co) in zip(up, ((dY, cfg_g, Gr, Gc), (X, cfg_x, Xr, Xc), (W, cfg_w, Wr, Wc))):
             stream.wait_event(u)
             fp4q.rht_quantize(x, cfg, ro, co, status=status, stream=stream)
         e1.record(stream)
@@ -286,6 +289,20 @@ def run_ours(args, world, rank, local):
             e2e_g.append(e1.elapsed_time(e2) * 1e-3)
     e2e_value = aggregate(q_bytes, sum(e2e_q) / len(e2e_q), world, dev) / 1e9
     e2e_gemm = aggregate(flops, sum(e2e_g) / len(e2e_g), world, dev) / 1e12
+    # the link alone: the same uploads and downloads with no compute (median of 5)
+    link = {}
+    for name, pairs in (("h2d", ((dY, hdY), (X, hX), (W, hW))), ("d2h", ((hY, Y), (hdX, dX), (hdW, dW)))):
+        ts = []
+        for _ in range(5):
+            a, b = ev(), ev()
+            a.record(copy_stream)
+            with torch.cuda.stream(copy_stream):
+                for dst, src in pairs:
+                    dst.copy_(src, non_blocking=True)
+            b.record(copy_stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b) * 1e-3)
+        link[name] = (h2d if name == "h2d" else d2h) / sorted(ts)[2] / 1e9
 
     # ---------------- rooflines of the two kernels (per-launch averages)
     g_launch = statistics.mean(kg["fprop"] + kg["dgrad"] + kg["wgrad"])
@@ -323,8 +340,10 @@ def run_ours(args, world, rank, local):
         "roofline_other": roof_q if dominant_gemm else roof_gemm,
         "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "gemm_tflops": round(e2e_gemm, 1),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": "H2D of X/W/dY inside the quantize phase, D2H of Y/dX/dW inside the GEMM phase; copies on a "
-                        "second stream overlap the compute that does not depend on them"},
+                "link_h2d_gb_s": round(link["h2d"], 1), "link_d2h_gb_s": round(link["d2h"], 1),
+                "note": "H2D of dY/X/W (in that order) inside the quantize phase, D2H of Y/dX/dW inside the GEMM "
+                        "phase; copies on a second stream overlap the compute that does not depend on them; "
+                        "link_*: the same copies alone"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "wall_s_timed": round(wall, 4),
