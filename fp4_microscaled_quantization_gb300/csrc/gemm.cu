@@ -736,12 +736,13 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
             }
             float2 P[16];
             chunk_from_bf16_words(w, p.q_sgn, P);
-            if (p.q_nh == 16) rotate_chunk<16>(P);
+            // MX output scales: H16's 1/4 goes into the power-of-two block scale
+            if (p.q_nh == 16) rotate_chunk<16, false>(P);
             else if (p.q_nh == 32) rotate_chunk<32>(P);
             ChunkOut o;
             const int64_t col = (int64_t)n0 + c0;
             quantize_chunk<QG, FP4Q_SCALE_MX, QR>(P, 0.0f, (uint64_t)(row * p.N + col), 0u, p.q_keys,
-                                                  p.q_e4m3 != nullptr, p.status, o);
+                                                  p.q_e4m3 != nullptr, p.status, o, p.q_nh == 16 ? 2 : 0);
             *reinterpret_cast<uint4*>(p.q_codes + row * (p.N / 2) + col / 2) = make_uint4(o.w[0], o.w[1], o.w[2], o.w[3]);
             const int64_t nkb = p.N / 32, k = col / 32;
             p.q_scales[p.q_sf_mma ? sf_mma_offset(row, k, nkb) : row * nkb + k] = (uint8_t)o.sbytes;

@@ -248,6 +248,8 @@ template <int GRID, int SCALE, int NH, int ROUND>
 __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
     rht_quant_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
   constexpr float kDen = 448.0f * GridK<GRID>::kQmax;
+  // MX with H16: the rotation's 1/4 goes into the power-of-two block scale
+  constexpr bool kFoldQuarter = SCALE == FP4Q_SCALE_MX && NH == 16;
   float S_row = 0.0f, S_col = 0.0f;
   if constexpr (SCALE == FP4Q_SCALE_NV) {
     if (p.want_row) S_row = __fdiv_rn(p.gamax[0], kDen);
@@ -269,10 +271,10 @@ __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
       if (c < p.cols && tr0 < p.rows) {
         float2 P[16];
         read_col_chunk(tv, threadIdx.x, p.sgn_col, P);
-        rotate_chunk<NH>(P);
+        rotate_chunk<NH, !kFoldQuarter>(P);
         ChunkOut o;
         quantize_chunk<GRID, SCALE, ROUND>(P, S_col, (uint64_t)(c * p.rows + tr0), 1u, p.sr_keys,
-                                           p.emit_e4m3, p.status, o);
+                                           p.emit_e4m3, p.status, o, kFoldQuarter ? 2 : 0);
         store_chunk<SCALE>(p.col, c, tr0, p.rows, p.sf_mma, p.emit_e4m3, o);
       }
     }
@@ -283,10 +285,10 @@ __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
       if (gr < p.rows && gc < p.cols) {
         float2 P[16];
         read_row_chunk(tv, r, q, p.sgn_row, P);
-        rotate_chunk<NH>(P);
+        rotate_chunk<NH, !kFoldQuarter>(P);
         ChunkOut o;
         quantize_chunk<GRID, SCALE, ROUND>(P, S_row, (uint64_t)(gr * p.cols + gc), 0u, p.sr_keys,
-                                           p.emit_e4m3, p.status, o);
+                                           p.emit_e4m3, p.status, o, kFoldQuarter ? 2 : 0);
         store_chunk<SCALE>(p.row, gr, gc, p.cols, p.sf_mma, p.emit_e4m3, o);
       }
     }

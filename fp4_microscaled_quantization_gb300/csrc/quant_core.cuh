@@ -129,7 +129,9 @@ __device__ __forceinline__ uint2 codes_to_e4m3(uint32_t w) {
 
 // ------------------------------------------------------------ one chunk
 // Rotation of a chunk held as P[i] = (u[i], u[i+16]) (signs already applied).
-template <int NH>
+// NORM = false leaves out H16's final multiply by 1/4, for an MX quantizer
+// that folds the 1/4 into its power-of-two block scale (quantize_chunk's pre).
+template <int NH, bool NORM = true>
 __device__ __forceinline__ void rotate_chunk(float2 (&P)[16]) {
   if constexpr (NH == 16 || NH == 32) {
 #pragma unroll
@@ -151,8 +153,10 @@ __device__ __forceinline__ void rotate_chunk(float2 (&P)[16]) {
       }
     }
     const float c = (NH == 16) ? 0.25f : __uint_as_float(0x3E3504F3u);  // fl32(1/sqrt(32))
+    if constexpr (NORM || NH != 16) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) P[i] = mul2(P[i], make_float2(c, c));
+      for (int i = 0; i < 16; ++i) P[i] = mul2(P[i], make_float2(c, c));
+    }
   }
 }
 
@@ -181,10 +185,17 @@ struct ChunkOut {
 // Scale, round and pack one rotated chunk.
 //   S_t    NV tensor scale (ignored for MX)
 //   idx0   index of element 0 in the stored copy (multiple of 32), for SR
+//   pre    MX only: P holds 2^pre times the rotated values (pre = 2 when
+//          H16's 1/4 was left out).  Exact for bf16 inputs: their unscaled
+//          H16 sums are multiples of 2^-133, so y = P / 4 has no rounding,
+//          the block exponent of P is that of y plus pre (also for
+//          subnormal blocks, pre being taken off before the clamp), and
+//          v = P 2^(127 - pre - sb) is the same real number as y 2^(127 - sb)
+//          with the same single rounding.
 template <int GRID, int SCALE, int ROUND>
 __device__ __forceinline__ void quantize_chunk(float2 (&P)[16], float S_t, uint64_t idx0,
                                                uint32_t orient, const uint32_t (&rk)[20],
-                                               bool emit_e4m3, uint32_t* status, ChunkOut& o) {
+                                               bool emit_e4m3, uint32_t* status, ChunkOut& o, int pre = 0) {
   constexpr float QMAX = GridK<GRID>::kQmax;
   // block amax (NaN-propagating)
   float m0 = 0.0f, m1 = 0.0f;
@@ -200,10 +211,12 @@ __device__ __forceinline__ void quantize_chunk(float2 (&P)[16], float S_t, uint6
     const float m = fabsf(absmax_nan(m0, m1));
     const uint32_t mb = __float_as_uint(m);
     if (mb >= 0x7F800000u) raise_status(status, FP4Q_DEV_NONFINITE);
-    int sb = (int)(mb >> 23) - GridK<GRID>::kEmax;   // floor(log2 m) - e_max + 127, 0 for m = 0
+    int sb = (int)(mb >> 23) - GridK<GRID>::kEmax - pre;   // floor(log2 m) - e_max + 127, 0 for m = 0
     sb = sb < 0 ? 0 : (sb > 254 ? 254 : sb);
-    // 2^-e = 2^(127 - sb): exponent field 254 - sb, or 2^-127 (subnormal) at sb = 254
-    const float mul = (sb < 254) ? __uint_as_float((uint32_t)(254 - sb) << 23) : __uint_as_float(0x00400000u);
+    // 2^-e 2^-pre = 2^(127 - pre - sb): exponent field z = 254 - pre - sb, or
+    // the subnormal 2^(z - 127) = 1 << (z + 22) for z <= 0 (z >= -2)
+    const int z = 254 - pre - sb;
+    const float mul = (z >= 1) ? __uint_as_float((uint32_t)z << 23) : __uint_as_float(1u << (z + 22));
     vm = make_float2(mul, mul);
     o.sbytes = (uint32_t)sb;
   } else {
