@@ -69,6 +69,13 @@ constexpr int A_BYTES = BM * KROW;   // 16 KB
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;      // accumulator columns [0, 256); scale columns after it
 
+// Epilogue warps of the plain kernels: 8 (two per TMEM lane quarter) or 16 (four).
+#ifndef FP4Q_GEMM_EPI_WARPS
+#define FP4Q_GEMM_EPI_WARPS 8
+#endif
+static_assert(FP4Q_GEMM_EPI_WARPS == 8 || FP4Q_GEMM_EPI_WARPS == 16, "FP4Q_GEMM_EPI_WARPS");
+constexpr int kPlainBoxBytes = FP4Q_GEMM_EPI_WARPS == 16 ? 32 : 64;   // staging box row of a plain epilogue warp
+
 template <int KIND, bool PAIR, bool FUSED = false>
 struct KindK {
   // chunks = 512-byte groups of 4 consecutive scale bytes of one 128-row group
@@ -89,12 +96,14 @@ struct KindK {
   static constexpr int kSfCols = KIND == KIND_MXF4 ? 32 : (KIND == KIND_NVF4 ? 64 : 16);
   static constexpr int kStage = (A_BYTES + kBBytes + kCompact + 1023) / 1024 * 1024;
   // threads: producer, MMA, scale-writer warps and the epilogue warps (4,
-  // or 8 when two drain each TMEM lane quarter)
-  static constexpr int kEpiWarps = FUSED ? 4 : 8;
+  // or 8 / 16 when two / four drain each TMEM lane quarter)
+  static constexpr int kEpiWarps = FUSED ? 4 : FP4Q_GEMM_EPI_WARPS;
   static constexpr int kThreads = 32 * (6 + kEpiWarps);
-  // epilogue staging per warp: one 32-row x 64-byte store box, or (fused
-  // output quantization) the warp's whole 32 x 256 bf16 slice of the tile
-  static constexpr int kStgWarp = FUSED ? 16384 : 2048;
+  static constexpr int kEpiCols = 256 / (kEpiWarps / 4);   // accumulator columns per epilogue warp
+  // epilogue staging per warp: one 32-row store box of kBoxBytes-byte rows, or
+  // (fused output quantization) the warp's whole 32 x 256 bf16 slice of the tile
+  static constexpr int kBoxBytes = FUSED ? 128 : kPlainBoxBytes;
+  static constexpr int kStgWarp = FUSED ? 16384 : 32 * kBoxBytes;
   static constexpr int kStagesMax = (232448 - 1280 - kEpiWarps * kStgWarp) / kStage;
   static constexpr int kStagesCap = kStagesMax > 6 ? 6 : kStagesMax;
   static constexpr int kStagesTmem = (int)(TMEM_COLS - BN) / kSfCols;   // stages whose scales fit beside the accumulator
@@ -652,14 +661,17 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
     // ---------------- epilogue (warps 2..5 and 10..13 -> TMEM lane quarters 2, 3, 0, 1)
     const int sp = warp & 3;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * sp) << 16) + ACC_COL;
-    const int epi = warp < 6 ? warp - 2 : warp - 6;                 // 0..7
+    const int grp = warp < 6 ? 0 : (warp - 6) >> 2;                // warps 2-5, 10-13, 14-17, 18-21
+    const int epi = grp * 4 + ((warp - 2) & 3);
     const uint32_t stg = stg_base + (uint32_t)epi * KK::kStgWarp;
-    // fused kernels: 128B-swizzled 32 x 64 bf16 boxes, 16-byte unit u of row
-    // `lane` at unit u ^ (lane & 7); plain kernels: 64B-swizzled 32-row x
-    // 64-byte boxes, unit u of row `lane` at unit u ^ ((lane >> 1) & 3)
-    const uint32_t row_off = (QG >= 0 ? 128u : 64u) * (uint32_t)lane;
-    const uint32_t swz = QG >= 0 ? (uint32_t)(lane & 7) : (uint32_t)((lane >> 1) & 3);
-    const int cbase = warp >= 10 ? 128 : 0;                         // this warp's accumulator columns
+    // swizzled boxes of 32 rows: 16-byte unit u of row `lane` sits at unit
+    // u ^ (lane & 7) with 128-byte rows (fused kernels), u ^ ((lane >> 1) & 3)
+    // with 64-byte rows, u ^ ((lane >> 2) & 1) with 32-byte rows
+    constexpr uint32_t BOXB = KK::kBoxBytes;
+    const uint32_t row_off = BOXB * (uint32_t)lane;
+    const uint32_t swz = BOXB == 128 ? (uint32_t)(lane & 7)
+                                     : (BOXB == 64 ? (uint32_t)((lane >> 1) & 3) : (uint32_t)((lane >> 2) & 1));
+    const int cbase = grp * KK::kEpiCols;                          // this warp's accumulator columns
     float alpha = 1.0f;
     if constexpr (KIND == KIND_NVF4) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
     uint32_t tl = 0;
@@ -755,9 +767,11 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
         }
         continue;
       }
-      uint32_t h[64];   // this warp's 128 columns of the row as packed bf16
+      constexpr int ECOLS = KK::kEpiCols, UNITS = (int)BOXB / 16;   // 16-byte units per box row
+      constexpr int FCOLS = (int)BOXB / 4, HCOLS = (int)BOXB / 2;   // columns of an fp32 / bf16 box
+      uint32_t h[ECOLS / 2];   // this warp's columns of the row as packed bf16
 #pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+      for (int c0 = 0; c0 < ECOLS; c0 += 32) {
         if (cbase + c0 < ncols) {
           uint32_t r[32];
           tmem_ld32(lane_base + (uint32_t)(cbase + c0), r);
@@ -766,20 +780,20 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
             for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), alpha));
           }
           if (p.want_f32 && live) {
-            // two 32-row x 16-float boxes per 32 columns
+            // 32-row x FCOLS-float boxes
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
+            for (int hh = 0; hh < 32 / FCOLS; ++hh) {
               if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
               __syncwarp();
 #pragma unroll
-              for (int u = 0; u < 4; ++u)
+              for (int u = 0; u < UNITS; ++u)
                 st_shared16(stg + row_off + 16u * ((uint32_t)u ^ swz),
-                            make_uint4(r[16 * hh + 4 * u], r[16 * hh + 4 * u + 1], r[16 * hh + 4 * u + 2],
-                                       r[16 * hh + 4 * u + 3]));
+                            make_uint4(r[FCOLS * hh + 4 * u], r[FCOLS * hh + 4 * u + 1], r[FCOLS * hh + 4 * u + 2],
+                                       r[FCOLS * hh + 4 * u + 3]));
               asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
               __syncwarp();
               if (lane == 0) {
-                tma_store_2d(&tmDf, n0 + cbase + c0 + 16 * hh, y, stg);
+                tma_store_2d(&tmDf, n0 + cbase + c0 + FCOLS * hh, y, stg);
                 asm volatile("cp.async.bulk.commit_group;" ::: "memory");
               }
             }
@@ -799,21 +813,21 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
         else mbar_arrive(lead_acc_empty);
       }
       if (p.want_bf16 && live) {
-        // one 32-row x 32-bf16 box per 32 columns
+        // 32-row x HCOLS-bf16 boxes
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          if (cbase + 32 * b < ncols) {
+        for (int b = 0; b < ECOLS / HCOLS; ++b) {
+          if (cbase + HCOLS * b < ncols) {
             if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             __syncwarp();
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < UNITS; ++u)
               st_shared16(stg + row_off + 16u * ((uint32_t)u ^ swz),
-                          make_uint4(h[16 * b + 4 * u], h[16 * b + 4 * u + 1], h[16 * b + 4 * u + 2],
-                                     h[16 * b + 4 * u + 3]));
+                          make_uint4(h[(HCOLS / 2) * b + 4 * u], h[(HCOLS / 2) * b + 4 * u + 1],
+                                     h[(HCOLS / 2) * b + 4 * u + 2], h[(HCOLS / 2) * b + 4 * u + 3]));
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tmDh, n0 + cbase + 32 * b, y, stg);
+              tma_store_2d(&tmDh, n0 + cbase + HCOLS * b, y, stg);
               asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             }
           }
@@ -842,12 +856,14 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t row
   return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, (uint32_t)KROW,
                         box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
-// Output [M][N] of bf16 or fp32, boxes of 32 rows x box_bytes (64 with 64B
-// swizzle for the plain kernels, 128 with 128B swizzle for the fused ones).
+// Output [M][N] of bf16 or fp32, boxes of 32 rows x box_bytes with the
+// swizzle of that row size (32 or 64 bytes for the plain kernels, 128 for the
+// fused ones).
 bool make_out_map(CUtensorMap* m, const void* base, uint64_t N, uint64_t M, bool f32, uint32_t box_bytes) {
   return encode_tmap_2d(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, N, M,
                         N * (f32 ? 4u : 2u), box_bytes / (f32 ? 4u : 2u), 32u,
-                        box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
+                        box_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                        : (box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B));
 }
 
 template <int KIND, int CL, int QG = -1, int QR = FP4Q_RTNE>
@@ -951,8 +967,9 @@ int32_t prepare_gemm(const fp4q_operand* A, const fp4q_operand* B, int64_t M, in
   if (!make_map(&ta, a_data, row_bytes, (uint64_t)M, BM) ||
       !make_map(&tb, b_data, row_bytes, (uint64_t)N, cl == CL_SINGLE ? 256u : 128u))
     return FP4Q_ERR_CUDA;
-  if (D_bf16 && !make_out_map(&tdh, D_bf16, (uint64_t)N, (uint64_t)M, false, fused ? 128u : 64u)) return FP4Q_ERR_CUDA;
-  if (D_f32 && !make_out_map(&tdf, D_f32, (uint64_t)N, (uint64_t)M, true, 64u)) return FP4Q_ERR_CUDA;
+  if (D_bf16 && !make_out_map(&tdh, D_bf16, (uint64_t)N, (uint64_t)M, false, fused ? 128u : (uint32_t)kPlainBoxBytes))
+    return FP4Q_ERR_CUDA;
+  if (D_f32 && !make_out_map(&tdf, D_f32, (uint64_t)N, (uint64_t)M, true, (uint32_t)kPlainBoxBytes)) return FP4Q_ERR_CUDA;
   return FP4Q_OK;
 }
 
