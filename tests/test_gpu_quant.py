@@ -125,6 +125,36 @@ def test_nv_given_amax_and_amax_pass(fq, orc):
         run_case(fq, orc, x, cfg, given=[float(g[0]) * 1.5, float(g[1]) * 0.5])   # caller's G (saturating too)
 
 
+def top_of_range_input(top_exp: int) -> np.ndarray:
+    """Rows 0-31: equal-sign 2^top_exp (1 + k/8); rows 32-47: normals times
+    2^100..2^(top_exp - 3); row 48: half 2^(top_exp - 1), half 1e-38."""
+    R, C = 64, 256
+    g = np.random.default_rng(77 + top_exp)
+    x = g.standard_normal((R, C)).astype(np.float32)
+    x[0:32, :] = np.float32(2.0 ** top_exp) * (1 + g.integers(0, 8, (32, C)).astype(np.float32) / 8)
+    x[32:48, :] *= np.float32(2.0) ** g.integers(100, top_exp - 2, (16, 1)).astype(np.float32)
+    x[48, :128] = np.float32(2.0 ** (top_exp - 1))
+    x[48, 128:] = np.float32(1e-38)
+    return synth.to_bf16_bits(x)
+
+
+@pytest.mark.parametrize("grid,rnd", [(0, 0), (1, 0), (2, 0), (1, 1), (0, 1)])
+def test_quantize_top_of_range(fq, orc, grid, rnd):
+    """Blocks whose rotated values reach the top of the fp32 range, without
+    overflowing it (a rotation overflow is a non-finite block, flagged by the
+    kernel).  With H16 and MX scales the kernel leaves the rotation's 1/4 to
+    the block scale, whose multiplier 2^(125 - sb) is subnormal when the
+    unscaled sums reach 2^127 (E1M2, scale byte 252): 16 equal-sign values
+    2^123 (1 + k/8) sum to [2^127, 2^128) under the deterministic H16.  H32
+    takes 2^122 so that its 32-term sums stay finite."""
+    for rot, top, masks in ((16, 123, ((0, 0), (0x5A5A, 0xA5A5))), (32, 122, ((0, 0),))):
+        bits = top_of_range_input(top)
+        for mr, mc in masks:
+            cfg = fq.Config(grid=grid, scale=0, rot=rot, round=rnd, sign_mask_row=mr, sign_mask_col=mc, sr_seed=99,
+                            emit_e4m3=(grid == 1))
+            run_case(fq, orc, bits, cfg)
+
+
 def test_empty_and_nonfinite(fq, orc):
     x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
     ro, co = fq.rht_quantize(x, fq.Config())
