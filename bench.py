@@ -28,6 +28,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -89,7 +90,9 @@ class ClockSampler:
     def __init__(self, bus_id: str | None):
         self.bus_id = bus_id
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # raw samples; the summary goes into the JSON line
+        log_dir = os.environ.get("FP4Q_BENCH_LOG_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(log_dir, f"fp4q_clocks_{os.getpid()}.csv")
 
     def start(self):
         os.makedirs(os.path.dirname(self.path), exist_ok=True)

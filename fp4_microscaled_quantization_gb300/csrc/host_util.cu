@@ -1,6 +1,6 @@
 // host_util.cu -- host-side helpers shared by the launchers: TMA tensor-map
-// encoding (through the driver entry point, so the library needs no link-time
-// libcuda) and a per-device SM count.
+// encoding (cuTensorMapEncodeTiled looked up with cudaGetDriverEntryPointByVersion, so
+// the library needs no link-time libcuda) and a per-device SM count.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
