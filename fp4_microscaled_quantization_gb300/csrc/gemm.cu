@@ -50,6 +50,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <type_traits>
+
 #include "../../include/fp4q.h"
 #include "fp4q_dev.cuh"
 #include "fp4q_internal.h"
@@ -134,6 +136,32 @@ struct GemmParams {
   int32_t q_nh, q_sf_mma;
   uint32_t q_sgn[32];     // sign words of a 32-element chunk (bit 31 = negate)
 };
+
+// Several GEMMs of one kind in one persistent launch (the plain single-CTA
+// kernels only): each CTA walks its own list of global tile ids, made on the
+// host so that the CTAs' summed tile costs are balanced (tiles of a long-K
+// GEMM cost more).  Passed by value as one kernel parameter.
+constexpr int kGroupMax = 4;          // GEMMs per launch
+constexpr int kGroupMaxUnits = 256;   // CTAs
+constexpr int kGroupMaxTiles = 8192;  // tiles of all the GEMMs together
+struct GroupArgs {
+  CUtensorMap a[kGroupMax], b[kGroupMax], dh[kGroupMax], df[kGroupMax];
+  const uint8_t* sfa[kGroupMax];
+  const uint8_t* sfb[kGroupMax];
+  const float* ts_a[kGroupMax];
+  const float* ts_b[kGroupMax];
+  int32_t M[kGroupMax], N[kGroupMax], K[kGroupMax];
+  int32_t want_bf16[kGroupMax], want_f32[kGroupMax];
+  int32_t tile0[kGroupMax + 1];       // first global tile id of each GEMM; tile0[np] = all tiles
+  int32_t np;
+  uint16_t unit_begin[kGroupMaxUnits + 1];   // CTA u walks order[unit_begin[u] .. unit_begin[u + 1])
+  uint16_t order[kGroupMaxTiles];
+};
+struct NoGroupArgs {
+  int32_t unused;
+};
+template <bool G>
+using GroupArg = std::conditional_t<G, GroupArgs, NoGroupArgs>;
 
 // ------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -391,11 +419,14 @@ __device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, 
 // A stage's ring slot is refilled only after both CTAs' MMAs released it:
 // every commit arrives on the empty barrier of both CTAs.
 // Tile id -> (m block = id / n_blocks, n block = id % n_blocks).
-template <int KIND, int CL, int QG = -1, int QR = FP4Q_RTNE>
+// GROUP: the GEMMs of `ga` instead of the one of (tmA, tmB, tmDh, tmDf, p);
+// p then only supplies the status word.
+template <int KIND, int CL, int QG = -1, int QR = FP4Q_RTNE, bool GROUP = false>
 __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThreads, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmDh, const __grid_constant__ CUtensorMap tmDf,
-                   const GemmParams p) {
+                   const GemmParams p, const __grid_constant__ GroupArg<GROUP> ga) {
+  static_assert(!GROUP || (CL == CL_SINGLE && QG < 0), "grouped launches use the plain single-CTA kernel");
   constexpr bool PAIR = CL == CL_PAIR, MC = CL == CL_MC, CLU = CL != CL_SINGLE;
   using KK = KindK<KIND, PAIR, (QG >= 0)>;
   constexpr int S = KK::kStages;
@@ -424,8 +455,68 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
   const int n_units = CLU ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   const int n_blocks = (p.N + BN - 1) / BN;
   const int n_tiles = ((p.M + TM - 1) / TM) * n_blocks;
-  const int num_kt = (p.K + KK::kElemsPerTile - 1) / KK::kElemsPerTile;
-  const int nq = p.K / KK::kBlock / 4;   // scale chunks per 128-row group
+
+  // The tiles this CTA walks, by work index w in [w_begin, w_end) step w_step,
+  // and what a tile needs: its GEMM (gi), corner, shape and K-tile count.
+  struct TileCtx {
+    int gi, m0, n0, M, N, K, num_kt, nq;
+  };
+  int w_begin = unit, w_end = n_tiles, w_step = n_units;
+  if constexpr (GROUP) {
+    w_begin = ga.unit_begin[unit];
+    w_end = ga.unit_begin[unit + 1];
+    w_step = 1;
+  }
+  auto tile_ctx = [&](int w) -> TileCtx {
+    TileCtx t;
+    int tile = w, nb = n_blocks;
+    if constexpr (GROUP) {
+      const int g = ga.order[w];
+      int gi = 0;
+#pragma unroll
+      for (int q = 1; q < kGroupMax; ++q) gi += (q < ga.np && g >= ga.tile0[q]) ? 1 : 0;
+      t.gi = gi;
+      t.M = ga.M[gi];
+      t.N = ga.N[gi];
+      t.K = ga.K[gi];
+      tile = g - ga.tile0[gi];
+      nb = (t.N + BN - 1) / BN;
+    } else {
+      t.gi = 0;
+      t.M = p.M;
+      t.N = p.N;
+      t.K = p.K;
+    }
+    t.m0 = (tile / nb) * TM + BM * (int)rank;
+    t.n0 = (tile % nb) * BN;
+    t.num_kt = (t.K + KK::kElemsPerTile - 1) / KK::kElemsPerTile;
+    t.nq = t.K / KK::kBlock / 4;   // scale chunks per 128-row group
+    return t;
+  };
+  auto map_a = [&](int gi) -> const CUtensorMap* {
+    if constexpr (GROUP) return &ga.a[gi];
+    else return &tmA;
+  };
+  auto map_b = [&](int gi) -> const CUtensorMap* {
+    if constexpr (GROUP) return &ga.b[gi];
+    else return &tmB;
+  };
+  auto map_dh = [&](int gi) -> const CUtensorMap* {
+    if constexpr (GROUP) return &ga.dh[gi];
+    else return &tmDh;
+  };
+  auto map_df = [&](int gi) -> const CUtensorMap* {
+    if constexpr (GROUP) return &ga.df[gi];
+    else return &tmDf;
+  };
+  auto sfa_of = [&](int gi) -> const uint8_t* {
+    if constexpr (GROUP) return ga.sfa[gi];
+    else return p.sfa;
+  };
+  auto sfb_of = [&](int gi) -> const uint8_t* {
+    if constexpr (GROUP) return ga.sfb[gi];
+    else return p.sfb;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -466,14 +557,26 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- producer
-      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
+      if constexpr (GROUP) {
+        for (int q = 0; q < ga.np; ++q) {
+          asm volatile("prefetch.tensormap [%0];" ::"l"(&ga.a[q]) : "memory");
+          asm volatile("prefetch.tensormap [%0];" ::"l"(&ga.b[q]) : "memory");
+        }
+      } else {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
+      }
       uint32_t it = 0;
-      for (int tile = unit; tile < n_tiles && !*abort_flag; tile += n_units) {
-        const int m0 = (tile / n_blocks) * TM + BM * (int)rank, n0 = (tile % n_blocks) * BN;
-        const bool rg1 = (n0 + 128) < p.N;   // the tile's second 128-row group of B exists
-        const bool rows = m0 < p.M;          // this CTA's rows of A exist (false only for a 128-row tail)
-        for (int kt = 0; kt < num_kt; ++kt, ++it) {
+      for (int w = w_begin; w < w_end && !*abort_flag; w += w_step) {
+        const TileCtx t = tile_ctx(w);
+        const int m0 = t.m0, n0 = t.n0, nq = t.nq;
+        const bool rg1 = (n0 + 128) < t.N;   // the tile's second 128-row group of B exists
+        const bool rows = m0 < t.M;          // this CTA's rows of A exist (false only for a 128-row tail)
+        const CUtensorMap* mA = map_a(t.gi);
+        const CUtensorMap* mB = map_b(t.gi);
+        const uint8_t* sfa_g = sfa_of(t.gi);
+        const uint8_t* sfb_g = sfb_of(t.gi);
+        for (int kt = 0; kt < t.num_kt; ++kt, ++it) {
           const int s = (int)(it % S);
           const uint32_t ph = (it / S) & 1u;
           if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag)) {
@@ -492,23 +595,23 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
           const uint32_t sf_tx = sf_bytes * ((rows ? 1u : 0u) + (rg1 ? 2u : 1u));
           if constexpr (PAIR) {
             remote_expect_tx(fb, A_BYTES + KK::kBBytes);
-            tma_load_2d_pair(st, &tmA, kt * KROW, m0, fb);
-            tma_load_2d_pair(st + A_BYTES, &tmB, kt * KROW, n0 + 128 * (int)rank, fb);
+            tma_load_2d_pair(st, mA, kt * KROW, m0, fb);
+            tma_load_2d_pair(st + A_BYTES, mB, kt * KROW, n0 + 128 * (int)rank, fb);
           } else if constexpr (MC) {
             // own A, own half of B into both CTAs; the peer's half lands here too
             mbar_expect_tx(fb, A_BYTES + KK::kBBytes + sf_tx);
-            tma_load_2d(st, &tmA, kt * KROW, m0, fb);
-            tma_load_2d_mc(st + A_BYTES + (uint32_t)(128 * KROW) * rank, &tmB, kt * KROW, n0 + 128 * (int)rank, fb);
+            tma_load_2d(st, mA, kt * KROW, m0, fb);
+            tma_load_2d_mc(st + A_BYTES + (uint32_t)(128 * KROW) * rank, mB, kt * KROW, n0 + 128 * (int)rank, fb);
           } else {
             mbar_expect_tx(fb, A_BYTES + KK::kBBytes + sf_tx);
-            tma_load_2d(st, &tmA, kt * KROW, m0, fb);
-            tma_load_2d(st + A_BYTES, &tmB, kt * KROW, n0, fb);
+            tma_load_2d(st, mA, kt * KROW, m0, fb);
+            tma_load_2d(st + A_BYTES, mB, kt * KROW, n0, fb);
           }
           if constexpr (PAIR) mbar_expect_tx(sb, sf_tx);
-          if (rows) bulk_load(st + SFA_OFF, p.sfa + ((size_t)(m0 / 128) * nq + q0) * 512, sf_bytes, sb);
-          bulk_load(st + SFA_OFF + KK::kChunks * 512, p.sfb + ((size_t)(n0 / 128) * nq + q0) * 512, sf_bytes, sb);
+          if (rows) bulk_load(st + SFA_OFF, sfa_g + ((size_t)(m0 / 128) * nq + q0) * 512, sf_bytes, sb);
+          bulk_load(st + SFA_OFF + KK::kChunks * 512, sfb_g + ((size_t)(n0 / 128) * nq + q0) * 512, sf_bytes, sb);
           if (rg1)
-            bulk_load(st + SFA_OFF + 2 * KK::kChunks * 512, p.sfb + ((size_t)(n0 / 128 + 1) * nq + q0) * 512,
+            bulk_load(st + SFA_OFF + 2 * KK::kChunks * 512, sfb_g + ((size_t)(n0 / 128 + 1) * nq + q0) * 512,
                       sf_bytes, sb);
         }
       }
@@ -541,7 +644,9 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
         if constexpr (PAIR) return mbar_wait(bar_full + 8 * ss, pp, abort_flag) && mbar_wait(bar_sf + 8 * ss, pp, abort_flag);
         else return mbar_wait(bar_sf + 8 * ss, pp, abort_flag);
       };
-      for (int tile = unit; tile < n_tiles && ok; tile += n_units, ++tl) {
+      for (int w = w_begin; w < w_end && ok; w += w_step, ++tl) {
+        const TileCtx t = tile_ctx(w);
+        const int num_kt = t.num_kt;
         ok = mbar_wait(bar_acc_empty, (tl & 1u) ^ 1u, abort_flag) && stage_ready(s, ph);
         if (!ok) break;
         for (int kt = 0; kt < num_kt; ++kt) {
@@ -549,7 +654,7 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
           const uint32_t st = sbase + s * KK::kStage;
           const uint32_t sfa_col = tmem + ACC_COL + BN + SF_COLS * s;
           const uint32_t sfb_col = sfa_col + KK::kSfColsA;
-          const int rem = p.K - kt * KK::kElemsPerTile;
+          const int rem = t.K - kt * KK::kElemsPerTile;
           const int n_mma = min(4, rem / KK::kMmaK);
           // descriptors of K slice k: the start address field advances by 32 bytes (2 units of 16)
           const uint64_t da = op_desc(st), db = op_desc(st + A_BYTES);
@@ -614,7 +719,8 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
     const uint32_t qbase = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     uint32_t it = 0;
     bool ok = true;
-    for (int tile = unit; tile < n_tiles && ok; tile += n_units) {
+    for (int w = w_begin; w < w_end && ok; w += w_step) {
+      const int num_kt = tile_ctx(w).num_kt;
       for (int kt = 0; kt < num_kt; ++kt, ++it) {
         const int s = (int)(it % S);
         const uint32_t ph = (it / S) & 1u;
@@ -673,12 +779,21 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
                                      : (BOXB == 64 ? (uint32_t)((lane >> 1) & 3) : (uint32_t)((lane >> 2) & 1));
     const int cbase = grp * KK::kEpiCols;                          // this warp's accumulator columns
     float alpha = 1.0f;
-    if constexpr (KIND == KIND_NVF4) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
+    if constexpr (KIND == KIND_NVF4 && !GROUP) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
     uint32_t tl = 0;
-    for (int tile = unit; tile < n_tiles; tile += n_units, ++tl) {
-      const int m0 = (tile / n_blocks) * TM + BM * (int)rank, n0 = (tile % n_blocks) * BN;
+    for (int w = w_begin; w < w_end; w += w_step, ++tl) {
+      const TileCtx t = tile_ctx(w);
+      const int m0 = t.m0, n0 = t.n0;
       const int y = m0 + 32 * sp;
-      const bool live = m0 < p.M;   // false only for the second CTA of a 128-row tail tile
+      const bool live = m0 < t.M;   // false only for the second CTA of a 128-row tail tile
+      const CUtensorMap* mDh = map_dh(t.gi);
+      const CUtensorMap* mDf = map_df(t.gi);
+      bool want_bf16 = p.want_bf16, want_f32 = p.want_f32;
+      if constexpr (GROUP) {
+        want_bf16 = ga.want_bf16[t.gi];
+        want_f32 = ga.want_f32[t.gi];
+        if constexpr (KIND == KIND_NVF4) alpha = __fmul_rn(*ga.ts_a[t.gi], *ga.ts_b[t.gi]);
+      }
       bool ok = mbar_wait(bar_acc_full, tl & 1u, abort_flag);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) {
@@ -689,7 +804,7 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
         break;
       }
       tc_fence_after();
-      const int ncols = min(BN, p.N - n0);   // 128 or 256
+      const int ncols = min(BN, t.N - n0);   // 128 or 256
       if constexpr (QG >= 0) {
         // Fused output quantization.  The warp's 32 x 256 bf16 slice goes to
         // shared memory as four swizzled 32 x 64 boxes (the previous tile's
@@ -779,7 +894,7 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), alpha));
           }
-          if (p.want_f32 && live) {
+          if (want_f32 && live) {
             // 32-row x FCOLS-float boxes
 #pragma unroll
             for (int hh = 0; hh < 32 / FCOLS; ++hh) {
@@ -793,7 +908,7 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
               asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
               __syncwarp();
               if (lane == 0) {
-                tma_store_2d(&tmDf, n0 + cbase + c0 + FCOLS * hh, y, stg);
+                tma_store_2d(mDf, n0 + cbase + c0 + FCOLS * hh, y, stg);
                 asm volatile("cp.async.bulk.commit_group;" ::: "memory");
               }
             }
@@ -812,7 +927,7 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
         if constexpr (PAIR) remote_arrive(lead_acc_empty);
         else mbar_arrive(lead_acc_empty);
       }
-      if (p.want_bf16 && live) {
+      if (want_bf16 && live) {
         // 32-row x HCOLS-bf16 boxes
 #pragma unroll
         for (int b = 0; b < ECOLS / HCOLS; ++b) {
@@ -827,7 +942,7 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tmDh, n0 + cbase + HCOLS * b, y, stg);
+              tma_store_2d(mDh, n0 + cbase + HCOLS * b, y, stg);
               asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             }
           }
@@ -914,7 +1029,113 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtens
   }
   if (tiles < units) units = tiles;
   cfg.gridDim = dim3((unsigned)(CLU ? 2 * units : units), 1, 1);
-  return cudaLaunchKernelEx(&cfg, bs_gemm_kernel<KIND, CL, QG, QR>, a, b, dh, df, p);
+  return cudaLaunchKernelEx(&cfg, bs_gemm_kernel<KIND, CL, QG, QR>, a, b, dh, df, p, NoGroupArgs{});
+}
+
+// One launch over the GEMMs of ga (plain single-CTA kernel); grid = the units
+// of ga's schedule.  p supplies the status word only.
+template <int KIND>
+cudaError_t launch_gemm_group(const GroupArgs& ga, int units, const GemmParams& p, cudaStream_t s) {
+  using KK = KindK<KIND, false, false>;
+  static unsigned attr_set = 0;   // one bit per device ordinal < 32
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned bit = dev < 32 ? (1u << dev) : 0u;
+  if (!(attr_set & bit) || !bit) {
+    e = cudaFuncSetAttribute(bs_gemm_kernel<KIND, CL_SINGLE, -1, FP4Q_RTNE, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, KK::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set |= bit;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)units, 1, 1);
+  cfg.blockDim = dim3(KK::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = KK::kSmem;
+  cfg.stream = s;
+  return cudaLaunchKernelEx(&cfg, bs_gemm_kernel<KIND, CL_SINGLE, -1, FP4Q_RTNE, true>, ga.a[0], ga.b[0], ga.dh[0],
+                            ga.df[0], p, ga);
+}
+
+// Static schedule of a grouped launch: tiles taken longest first (a tile
+// costs 4 per K-tile of 256 plus 10 for its epilogue, in about a quarter of a
+// stage's time), each given to the CTA with the least work so far (a binary
+// heap of CTA loads); every CTA's tiles are then stored together, in the
+// order it received them.  The last schedule is kept per host thread and
+// reused while the shapes and the CTA count repeat.  Returns the CTA count.
+int group_schedule(GroupArgs& ga, int units) {
+  const int total = ga.tile0[ga.np];
+  if (units > total) units = total;
+  if (units > kGroupMaxUnits) units = kGroupMaxUnits;
+  struct Cache {
+    int np = 0, units = 0;
+    int32_t M[kGroupMax], N[kGroupMax], K[kGroupMax];
+    uint16_t unit_begin[kGroupMaxUnits + 1];
+    uint16_t order[kGroupMaxTiles];
+  };
+  static thread_local Cache cache;
+  bool hit = cache.np == ga.np && cache.units == units;
+  for (int i = 0; hit && i < ga.np; ++i)
+    hit = cache.M[i] == ga.M[i] && cache.N[i] == ga.N[i] && cache.K[i] == ga.K[i];
+  if (!hit) {
+    int gorder[kGroupMax];
+    for (int i = 0; i < ga.np; ++i) gorder[i] = i;
+    auto cost = [&](int gi) { return (int64_t)4 * ((ga.K[gi] + 255) / 256) + 10; };
+    for (int i = 1; i < ga.np; ++i)   // GEMMs by decreasing tile cost (insertion sort, np <= 4)
+      for (int j = i; j > 0 && cost(gorder[j]) > cost(gorder[j - 1]); --j) {
+        const int t = gorder[j];
+        gorder[j] = gorder[j - 1];
+        gorder[j - 1] = t;
+      }
+    // min-heap of (load, unit); ties go to the lower unit
+    static thread_local int64_t hload[kGroupMaxUnits];
+    static thread_local int hunit[kGroupMaxUnits];
+    static thread_local uint16_t owner[kGroupMaxTiles], by_seq[kGroupMaxTiles];
+    static thread_local int count[kGroupMaxUnits + 1];
+    auto less = [&](int x, int y) { return hload[x] < hload[y] || (hload[x] == hload[y] && hunit[x] < hunit[y]); };
+    for (int u = 0; u < units; ++u) {
+      hload[u] = 0;
+      hunit[u] = u;
+    }
+    int seq = 0;
+    for (int i = 0; i < ga.np; ++i) {
+      const int gi = gorder[i];
+      for (int g = ga.tile0[gi]; g < ga.tile0[gi + 1]; ++g) {
+        owner[seq] = (uint16_t)hunit[0];
+        by_seq[seq++] = (uint16_t)g;
+        hload[0] += cost(gi);
+        for (int x = 0;;) {   // sift the root down
+          const int l = 2 * x + 1, r = l + 1;
+          int m = x;
+          if (l < units && less(l, m)) m = l;
+          if (r < units && less(r, m)) m = r;
+          if (m == x) break;
+          const int64_t tl = hload[x];
+          const int tu = hunit[x];
+          hload[x] = hload[m];
+          hunit[x] = hunit[m];
+          hload[m] = tl;
+          hunit[m] = tu;
+          x = m;
+        }
+      }
+    }
+    for (int u = 0; u <= units; ++u) count[u] = 0;
+    for (int k = 0; k < seq; ++k) ++count[owner[k] + 1];
+    for (int u = 0; u < units; ++u) count[u + 1] += count[u];
+    for (int u = 0; u <= units; ++u) cache.unit_begin[u] = (uint16_t)count[u];
+    for (int k = 0; k < seq; ++k) cache.order[count[owner[k]]++] = by_seq[k];
+    cache.np = ga.np;
+    cache.units = units;
+    for (int i = 0; i < ga.np; ++i) {
+      cache.M[i] = ga.M[i];
+      cache.N[i] = ga.N[i];
+      cache.K[i] = ga.K[i];
+    }
+  }
+  memcpy(ga.unit_begin, cache.unit_begin, sizeof(uint16_t) * (units + 1));
+  memcpy(ga.order, cache.order, sizeof(uint16_t) * total);
+  return units;
 }
 
 bool al(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -997,6 +1218,46 @@ extern "C" int32_t fp4q_gemm(const fp4q_operand* A, const fp4q_operand* B, int64
                                   kind, p, ta, tb, tdh, tdf);
   if (st != FP4Q_OK) return st;
   const cudaError_t e = launch_kind<-1, FP4Q_RTNE>(kind, ta, tb, tdh, tdf, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
+}
+
+extern "C" int32_t fp4q_gemm_group(const fp4q_gemm_problem* problems, int32_t count, int32_t grid, int32_t scale,
+                                   uint32_t* d_status, void* stream) {
+  using namespace fp4q;
+  if (!problems || count < 1 || count > kGroupMax) return FP4Q_ERR_INVALID_ARG;
+  static thread_local GroupArgs ga;   // ~19 KB: copied into the launch, reused by the next call
+  memset(&ga, 0, sizeof(GroupArgs));
+  ga.np = count;
+  ga.tile0[0] = 0;
+  int kind = KIND_MXF4;
+  GemmParams p0;
+  for (int i = 0; i < count; ++i) {
+    const fp4q_gemm_problem& q = problems[i];
+    if (!q.D_bf16 && !q.D_f32) return FP4Q_ERR_INVALID_ARG;
+    GemmParams pi;
+    const int32_t st = prepare_gemm(q.A, q.B, q.M, q.N, q.K, grid, scale, q.D_bf16, q.D_f32, d_status, CL_SINGLE,
+                                    false, kind, pi, ga.a[i], ga.b[i], ga.dh[i], ga.df[i]);
+    if (st != FP4Q_OK) return st;
+    if (i == 0) p0 = pi;
+    ga.sfa[i] = pi.sfa;
+    ga.sfb[i] = pi.sfb;
+    ga.ts_a[i] = pi.ts_a;
+    ga.ts_b[i] = pi.ts_b;
+    ga.M[i] = pi.M;
+    ga.N[i] = pi.N;
+    ga.K[i] = pi.K;
+    ga.want_bf16[i] = pi.want_bf16;
+    ga.want_f32[i] = pi.want_f32;
+    const int64_t tiles = (q.M / BM) * ((q.N + BN - 1) / BN);
+    if (ga.tile0[i] + tiles > kGroupMaxTiles) return FP4Q_ERR_UNSUPPORTED;
+    ga.tile0[i + 1] = ga.tile0[i] + (int32_t)tiles;
+  }
+  const int units = group_schedule(ga, num_sms());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (kind == KIND_MXF4) e = launch_gemm_group<KIND_MXF4>(ga, units, p0, s);
+  else if (kind == KIND_NVF4) e = launch_gemm_group<KIND_NVF4>(ga, units, p0, s);
+  else e = launch_gemm_group<KIND_F8>(ga, units, p0, s);
   return e == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
 }
 

@@ -47,6 +47,11 @@ class COperand(ctypes.Structure):
                 ("tensor_scale", ctypes.c_void_p), ("e4m3", ctypes.c_void_p)]
 
 
+class CGemmProblem(ctypes.Structure):
+    _fields_ = [("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("M", ctypes.c_int64), ("N", ctypes.c_int64),
+                ("K", ctypes.c_int64), ("D_bf16", ctypes.c_void_p), ("D_f32", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -78,6 +83,8 @@ def lib() -> ctypes.CDLL:
         L.fp4q_gemm.argtypes = [P, P, i64, i64, i64, i32, i32, P, P, P, P]
         L.fp4q_gemm_quantize.restype = i32
         L.fp4q_gemm_quantize.argtypes = [P, P, i64, i64, i64, i32, i32, P, P, P, P, P]
+        L.fp4q_gemm_group.restype = i32
+        L.fp4q_gemm_group.argtypes = [P, i32, i32, i32, P, P]
         L.fp4q_bias_stats_workspace_bytes.restype = sz
         L.fp4q_bias_stats_workspace_bytes.argtypes = [i64]
         L.fp4q_bias_stats.restype = i32
@@ -236,6 +243,31 @@ def gemm(A: Operand, B: Operand, grid: int, scale: int, want_bf16: bool = True, 
     _check("fp4q_gemm", lib().fp4q_gemm(ctypes.byref(ac), ctypes.byref(bc), M, N, K, grid, scale, _p(D_bf16),
                                          _p(D_f32), _p(status), _stream(stream)))
     return D_bf16, D_f32
+
+
+def gemm_group(pairs, grid: int, scale: int, want_bf16: bool = True, want_f32: bool = False, outs=None,
+               status=None, stream=None):
+    """Several GEMMs D_i = alpha_g * A_i B_i^T of one recipe in one launch
+    (fp4q_gemm_group).  pairs: [(A_i, B_i)]; outs: optional [(D_bf16, D_f32)].
+    Returns [(D_bf16, D_f32)] per GEMM."""
+    keep, probs, res = [], [], []
+    for i, (A, B) in enumerate(pairs):
+        M, K, N = A.rows, A.cols, B.rows
+        dev = A.codes.device
+        db, df = outs[i] if outs is not None else (None, None)
+        if db is None and want_bf16:
+            db = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        if df is None and want_f32:
+            df = torch.empty((M, N), dtype=torch.float32, device=dev)
+        ac, bc = A.c(), B.c()
+        keep += [ac, bc]
+        probs.append(CGemmProblem(ctypes.addressof(ac), ctypes.addressof(bc), M, N, K, _p(db), _p(df)))
+        res.append((db, df))
+    arr = (CGemmProblem * len(probs))(*probs)
+    _check("fp4q_gemm_group", lib().fp4q_gemm_group(ctypes.cast(arr, ctypes.c_void_p), len(probs), grid, scale,
+                                                     _p(status), _stream(stream)))
+    del keep
+    return res
 
 
 def gemm_quantize(A: Operand, B: Operand, grid: int, scale: int, out_cfg: Config, want_bf16: bool = False,

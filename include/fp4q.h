@@ -189,6 +189,27 @@ int32_t fp4q_gemm(const fp4q_operand* A, const fp4q_operand* B, int64_t M, int64
                   int32_t grid, int32_t scale, void* D_bf16, float* D_f32, uint32_t* d_status,
                   void* stream);
 
+/* Several block-scaled GEMMs of one recipe (grid, scale) in one launch, each
+ * exactly as fp4q_gemm computes it (the same tiles, bit for bit): for the
+ * GEMMs of one training phase, e.g. Dgrad and Wgrad of a linear layer, whose
+ * tiles cost differently (K), so that one persistent launch over a
+ * cost-balanced static tile list keeps every SM busy to the end.
+ *  problems  count descriptions, each as fp4q_gemm's arguments (A, B, M, N, K,
+ *           D_bf16, D_f32; at least one output each)
+ *  count    1 .. 4
+ *  Returns FP4Q_ERR_UNSUPPORTED when the GEMMs have more than 8192 128 x 256
+ *  tiles together (call fp4q_gemm for each then), otherwise as fp4q_gemm.
+ *  The outputs must not overlap one another or the inputs. */
+typedef struct {
+  const fp4q_operand* A;
+  const fp4q_operand* B;
+  int64_t M, N, K;
+  void* D_bf16;
+  float* D_f32;
+} fp4q_gemm_problem;
+int32_t fp4q_gemm_group(const fp4q_gemm_problem* problems, int32_t count, int32_t grid, int32_t scale,
+                        uint32_t* d_status, void* stream);
+
 /* The same GEMM, quantizing its own output in the epilogue: `out` receives
  * the row-wise copy of bf16(D) that fp4q_rht_quantize would produce from the
  * stored bf16 D with `out_cfg`, bit for bit, without D making a round trip
