@@ -39,7 +39,8 @@ SEED = 1005
 MX_BYTES_PER_ELEM = 2 + 2 * (0.5 + 1 / 32)     # bf16 in, two copies of codes + E8M0 scales
 WORKLOAD = ("one linear layer, bf16 X[16384,4096] W[4096,4096] dY[16384,4096]: fused random-H16 + "
             "MXFP4 E2M1 quantization of all three (row+col copies; RTNE X/W, Philox SR dY), then "
-            "Fprop Y=XW^T, Dgrad dX=dY W, Wgrad dW=dY^T X block-scaled FP4 GEMMs (bf16 out)")
+            "Fprop Y=XW^T, Dgrad dX=dY W, Wgrad dW=dY^T X block-scaled FP4 GEMMs (bf16 out; Dgrad and Wgrad in "
+            "one grouped launch)")
 
 
 # ------------------------------------------------------------------ ranks
@@ -170,11 +171,11 @@ def run_ours(args, world, rank, local):
 
     q_bytes = MX_BYTES_PER_ELEM * (TOKENS * D_IN + D_OUT * D_IN + TOKENS * D_OUT)
     flops = 3 * 2.0 * TOKENS * D_IN * D_OUT
-    launches_per_step = 6
+    launches_per_step = 5      # 3 quantizer launches, Fprop, the grouped Dgrad + Wgrad
 
     ev = lambda: torch.cuda.Event(enable_timing=True)
     kq = {"x": [], "w": [], "g": []}
-    kg = {"fprop": [], "dgrad": [], "wgrad": []}
+    kg = {"fprop": [], "dgrad_wgrad": []}
 
     def quantize_phase(rec=None):
         e = [ev() for _ in range(4)] if rec is not None else None
@@ -189,14 +190,14 @@ def run_ours(args, world, rank, local):
             rec.append(("q", e))
 
     def gemm_phase(rec=None):
-        e = [ev() for _ in range(4)] if rec is not None else None
+        # Fprop, then the backward GEMMs (Dgrad, Wgrad) in one grouped launch
+        e = [ev() for _ in range(3)] if rec is not None else None
         if e: e[0].record(stream)
         fp4q.gemm(Xr, Wr, fp4q.GRID_E2M1, fp4q.SCALE_MX, want_f32=False, D_bf16=Y, status=status, stream=stream)
         if e: e[1].record(stream)
-        fp4q.gemm(Gr, Wc, fp4q.GRID_E2M1, fp4q.SCALE_MX, want_f32=False, D_bf16=dX, status=status, stream=stream)
+        fp4q.gemm_group([(Gr, Wc), (Gc, Xc)], fp4q.GRID_E2M1, fp4q.SCALE_MX, want_bf16=True, want_f32=False,
+                        outs=[(dX, None), (dW, None)], status=status, stream=stream)
         if e: e[2].record(stream)
-        fp4q.gemm(Gc, Xc, fp4q.GRID_E2M1, fp4q.SCALE_MX, want_f32=False, D_bf16=dW, status=status, stream=stream)
-        if e: e[3].record(stream)
         if rec is not None:
             rec.append(("g", e))
 
@@ -234,9 +235,9 @@ def run_ours(args, world, rank, local):
 
     q_times, g_times = [], []
     for kind, e in recs:
-        per = [e[i].elapsed_time(e[i + 1]) * 1e-3 for i in range(3)]
+        per = [e[i].elapsed_time(e[i + 1]) * 1e-3 for i in range(len(e) - 1)]
         (q_times if kind == "q" else g_times).append(sum(per))
-        for key, t in zip(("x", "w", "g") if kind == "q" else ("fprop", "dgrad", "wgrad"), per):
+        for key, t in zip(("x", "w", "g") if kind == "q" else ("fprop", "dgrad_wgrad"), per):
             (kq if kind == "q" else kg)[key].append(t)
     q_s = sum(q_times) / len(q_times)
     g_s = sum(g_times) / len(g_times)
@@ -275,13 +276,20 @@ def run_ours(args, world, rank, local):
             stream.wait_event(u)
             fp4q.rht_quantize(x, cfg, ro, co, status=status, stream=stream)
         e1.record(stream)
-        for a, b, d, hd in ((Xr, Wr, Y, hY), (Gr, Wc, dX, hdX), (Gc, Xc, dW, hdW)):
-            fp4q.gemm(a, b, fp4q.GRID_E2M1, fp4q.SCALE_MX, want_f32=False, D_bf16=d, status=status, stream=stream)
-            g = ev()
-            g.record(stream)
-            copy_stream.wait_event(g)
-            with torch.cuda.stream(copy_stream):
-                hd.copy_(d, non_blocking=True)
+        fp4q.gemm(Xr, Wr, fp4q.GRID_E2M1, fp4q.SCALE_MX, want_f32=False, D_bf16=Y, status=status, stream=stream)
+        g = ev()
+        g.record(stream)
+        copy_stream.wait_event(g)
+        with torch.cuda.stream(copy_stream):
+            hY.copy_(Y, non_blocking=True)
+        fp4q.gemm_group([(Gr, Wc), (Gc, Xc)], fp4q.GRID_E2M1, fp4q.SCALE_MX, want_bf16=True, want_f32=False,
+                        outs=[(dX, None), (dW, None)], status=status, stream=stream)
+        g = ev()
+        g.record(stream)
+        copy_stream.wait_event(g)
+        with torch.cuda.stream(copy_stream):
+            hdX.copy_(dX, non_blocking=True)
+            hdW.copy_(dW, non_blocking=True)
         down = ev()
         down.record(copy_stream)
         stream.wait_event(down)
@@ -307,17 +315,23 @@ def run_ours(args, world, rank, local):
             ts.append(a.elapsed_time(b) * 1e-3)
         link[name] = (h2d if name == "h2d" else d2h) / sorted(ts)[2] / 1e9
 
-    # ---------------- rooflines of the two kernels (per-launch averages)
-    g_launch = statistics.mean(kg["fprop"] + kg["dgrad"] + kg["wgrad"])
-    g_achieved = 2.0 * TOKENS * D_IN * D_OUT / g_launch / 1e12
+    # ---------------- rooflines of the two kernels (per-launch averages).  The
+    # GEMM kernel runs twice a step (Fprop; Dgrad + Wgrad grouped): achieved =
+    # the step's GEMM flops / the two launches' summed durations, traffic = the
+    # mean of the two launches' measured DRAM bytes
+    g_achieved = flops / (statistics.mean(kg["fprop"]) + statistics.mean(kg["dgrad_wgrad"])) / 1e12
     x_launch = statistics.mean(kq["x"])
     x_bytes = MX_BYTES_PER_ELEM * TOKENS * D_IN
     x_achieved = x_bytes / x_launch / 1e9
     traffic = read_traffic()
     dominant_gemm = sum(g_times) >= sum(q_times)
-    roof_gemm = {"kernel": "bs_gemm_kernel<mxf4> (tcgen05)", "bound": "tensor", "achieved": round(g_achieved, 1),
+    g_traffic = None
+    if "gemm_mxf4_fprop_bytes" in traffic and "gemm_mxf4_group_dgrad_wgrad_bytes" in traffic:
+        g_traffic = (traffic["gemm_mxf4_fprop_bytes"] + traffic["gemm_mxf4_group_dgrad_wgrad_bytes"]) // 2
+    roof_gemm = {"kernel": "bs_gemm_kernel<mxf4> (tcgen05): Fprop launch + grouped Dgrad/Wgrad launch",
+                 "bound": "tensor", "achieved": round(g_achieved, 1),
                  "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(g_achieved / fp4_peak, 4),
-                 "traffic": traffic.get("gemm_mxf4_fprop_bytes"),
+                 "traffic": g_traffic,
                  "peak_source": f"{peak_src} bf16 burst x 6 (nominal FP4:BF16 dense ratio)"}
     roof_q = {"kernel": "rht_quant_kernel (X, both copies)", "bound": "hbm", "achieved": round(x_achieved, 1),
               "peak": hbm_peak, "unit": "GB/s", "frac": round(x_achieved / hbm_peak, 4),

@@ -88,8 +88,8 @@ class Fp4Linear:
         g = self.grid
         kw = dict(want_bf16=True, want_f32=self.out_f32, stream=stream)
         Yb, Yf = fp4q.gemm(q["Xr"], q["Wr"], g, fp4q.SCALE_MX, **kw)      # Fprop  [M, N]
-        dXb, dXf = fp4q.gemm(q["Gr"], q["Wc"], g, fp4q.SCALE_MX, **kw)    # Dgrad  [M, K]
-        dWb, dWf = fp4q.gemm(q["Gc"], q["Xc"], g, fp4q.SCALE_MX, **kw)    # Wgrad  [N, K]
+        # the backward GEMMs, Dgrad [M, K] and Wgrad [N, K], in one balanced launch
+        (dXb, dXf), (dWb, dWf) = fp4q.gemm_group([(q["Gr"], q["Wc"]), (q["Gc"], q["Xc"])], g, fp4q.SCALE_MX, **kw)
         if self.out_f32:
             return Yf, dXf, dWf
         return Yb, dXb, dWb
