@@ -41,6 +41,11 @@
 // tensor pipe free of scale copies (tcgen05.cp), which cost it 15-60 cycles
 // each, and needs no shared-memory staging.
 //
+// Grouped launches (fp4q_gemm_group) run the same kernel over the tiles of
+// several GEMMs of one recipe, each CTA walking its own host-made tile list
+// (longest tiles first, each to the least-loaded CTA), so that GEMMs with
+// different K keep every SM busy to the end of one launch.
+//
 // Every mbarrier wait is bounded (about 2 s of %globaltimer); on expiry the
 // CTA raises FP4Q_DEV_TIMEOUT, stops issuing work, waits (bounded) for its
 // own tensor-core work to drain, frees its TMEM and exits.
