@@ -66,8 +66,8 @@ namespace fp4q {
 namespace {
 
 enum { KIND_MXF4 = 0, KIND_NVF4 = 1, KIND_F8 = 2 };
-// CTA cooperation: none, a cta_group::2 pair, or a cluster of two that shares B by TMA multicast
-enum { CL_SINGLE = 0, CL_PAIR = 1, CL_MC = 2 };
+// CTA cooperation: none, or a cta_group::2 pair
+enum { CL_SINGLE = 0, CL_PAIR = 1 };
 
 constexpr int BM = 128;              // accumulator rows per CTA (TMEM lanes)
 constexpr int BN = 256;              // tile columns (MMA N)
@@ -367,24 +367,6 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
       "h"((uint16_t)3)
       : "memory");
 }
-// TMA load delivered to the same shared-memory offset, and completing on the
-// barrier at the same offset, in both CTAs of the cluster.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* tm, int32_t x, int32_t y,
-                                               uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
-      "[%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(tm), "r"(x), "r"(y), "r"(bar), "h"((uint16_t)3)
-      : "memory");
-}
-// Commit of this CTA's tensor-core work, arriving on the barrier at this
-// offset in both CTAs of the cluster.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"((uint16_t)3)
-      : "memory");
-}
 template <int KIND>
 __device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
                                             uint32_t sfb, uint32_t acc) {
@@ -417,12 +399,6 @@ __device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, 
 // 128r..128r+127 of the tile's B, and tcgen05.mma.cta_group::2 issued by rank
 // 0 (the leader) reads both CTAs' operands, so each SM moves 32 KB of A/B per
 // K-tile instead of 48 KB and its tensor core reads half of B from the peer.
-// Multicast cluster (CL_MC, clusters of two): the same 256 x 256 tiles, but
-// each CTA runs its own cta_group::1 MMAs on a full copy of B in its shared
-// memory; rank r loads B rows 128r..128r+127 once and TMA multicast writes
-// them into both CTAs, so each SM pulls 32 KB of A/B per K-tile out of L2.
-// A stage's ring slot is refilled only after both CTAs' MMAs released it:
-// every commit arrives on the empty barrier of both CTAs.
 // Tile id -> (m block = id / n_blocks, n block = id % n_blocks).
 // GROUP: the GEMMs of `ga` instead of the one of (tmA, tmB, tmDh, tmDf, p);
 // p then only supplies the status word.
@@ -432,7 +408,7 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
                    const __grid_constant__ CUtensorMap tmDh, const __grid_constant__ CUtensorMap tmDf,
                    const GemmParams p, const __grid_constant__ GroupArg<GROUP> ga) {
   static_assert(!GROUP || (CL == CL_SINGLE && QG < 0), "grouped launches use the plain single-CTA kernel");
-  constexpr bool PAIR = CL == CL_PAIR, MC = CL == CL_MC, CLU = CL != CL_SINGLE;
+  constexpr bool PAIR = CL == CL_PAIR, CLU = CL != CL_SINGLE;
   using KK = KindK<KIND, PAIR, (QG >= 0)>;
   constexpr int S = KK::kStages;
   constexpr int TM = CLU ? 256 : BM;                          // tile rows
@@ -526,7 +502,7 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full + 8 * s, PAIR ? 2 : 1);   // one expect_tx arrival per producer
-      mbar_init(bar_empty + 8 * s, MC ? 2 : 1);    // the (leader's) commit; both CTAs' in MC
+      mbar_init(bar_empty + 8 * s, 1);            // the (leader's) commit
       mbar_init(bar_sfd + 8 * s, 1);
       mbar_init(bar_sf + 8 * s, PAIR ? 8 : 4);     // one arrival per scale-writer warp
     }
@@ -602,11 +578,6 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
             remote_expect_tx(fb, A_BYTES + KK::kBBytes);
             tma_load_2d_pair(st, mA, kt * KROW, m0, fb);
             tma_load_2d_pair(st + A_BYTES, mB, kt * KROW, n0 + 128 * (int)rank, fb);
-          } else if constexpr (MC) {
-            // own A, own half of B into both CTAs; the peer's half lands here too
-            mbar_expect_tx(fb, A_BYTES + KK::kBBytes + sf_tx);
-            tma_load_2d(st, mA, kt * KROW, m0, fb);
-            tma_load_2d_mc(st + A_BYTES + (uint32_t)(128 * KROW) * rank, mB, kt * KROW, n0 + 128 * (int)rank, fb);
           } else {
             mbar_expect_tx(fb, A_BYTES + KK::kBBytes + sf_tx);
             tma_load_2d(st, mA, kt * KROW, m0, fb);
@@ -693,7 +664,6 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
             for (int k = 0; k < n_mma; ++k) issue(k);
           }
           if constexpr (PAIR) tc_commit_pair(bar_empty + 8 * s);
-          else if constexpr (MC) tc_commit_mc(bar_empty + 8 * s);
           else tc_commit(bar_empty + 8 * s);
           if (has_next) ok = stage_ready(s2, ph2);
           s = s2;
@@ -1145,14 +1115,14 @@ int group_schedule(GroupArgs& ga, int units) {
 
 bool al(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Cooperation form of the plain GEMM kernels, -DFP4Q_GEMM_CLUSTER=0/1/2:
-// single CTA, cta_group::2 pair, multicast cluster.  The fused-quantization
-// kernels use the single or multicast form (the pair form is not built for them).
+// Cooperation form of the plain GEMM kernels, -DFP4Q_GEMM_CLUSTER=0/1:
+// single CTA or cta_group::2 pair.  The fused-quantization kernels use the
+// single form (the pair form is not built for them).
 #ifndef FP4Q_GEMM_CLUSTER
 #define FP4Q_GEMM_CLUSTER 0
 #endif
 constexpr int kCluster = FP4Q_GEMM_CLUSTER;
-static_assert(kCluster == CL_SINGLE || kCluster == CL_PAIR || kCluster == CL_MC, "FP4Q_GEMM_CLUSTER");
+static_assert(kCluster == CL_SINGLE || kCluster == CL_PAIR, "FP4Q_GEMM_CLUSTER");
 template <int QG>
 constexpr int cluster_form() { return (kCluster == CL_PAIR && QG >= 0) ? CL_SINGLE : kCluster; }
 
@@ -1168,7 +1138,7 @@ int32_t prepare_gemm(const fp4q_operand* A, const fp4q_operand* B, int64_t M, in
   if (M <= 0 || N <= 0 || K <= 0) return FP4Q_ERR_INVALID_ARG;
   if (M % 128 || N % 128) return FP4Q_ERR_INVALID_ARG;
   if (K % (scale == FP4Q_SCALE_NV ? 64 : 128)) return FP4Q_ERR_INVALID_ARG;
-  if (M / 128 > 65535 || M > (1LL << 31) || N > (1LL << 31) || K > (1LL << 31)) return FP4Q_ERR_INVALID_ARG;
+  if (M / 128 > 65535 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP4Q_ERR_INVALID_ARG;
   kind = grid == FP4Q_GRID_E1M2 ? KIND_F8 : (scale == FP4Q_SCALE_NV ? KIND_NVF4 : KIND_MXF4);
   const void* a_data = kind == KIND_F8 ? (const void*)A->e4m3 : (const void*)A->codes;
   const void* b_data = kind == KIND_F8 ? (const void*)B->e4m3 : (const void*)B->codes;

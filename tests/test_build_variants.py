@@ -1,7 +1,6 @@
 """The GEMM's build options that are off by default still compile for sm_103a:
-the cta_group::2 pair form (-DFP4Q_GEMM_CLUSTER=1), the multicast cluster form
-(-DFP4Q_GEMM_CLUSTER=2) and sixteen epilogue warps (-DFP4Q_GEMM_EPI_WARPS=16).
-Compile only (no GPU); the three run in parallel."""
+the cta_group::2 pair form (-DFP4Q_GEMM_CLUSTER=1) and sixteen epilogue warps
+(-DFP4Q_GEMM_EPI_WARPS=16).  Compile only (no GPU); the two run in parallel."""
 import os
 import shutil
 import subprocess
@@ -11,7 +10,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 GEMM = os.path.join(ROOT, "fp4_microscaled_quantization_gb300", "csrc", "gemm.cu")
-VARIANTS = {"pair": "-DFP4Q_GEMM_CLUSTER=1", "multicast": "-DFP4Q_GEMM_CLUSTER=2", "epi16": "-DFP4Q_GEMM_EPI_WARPS=16"}
+VARIANTS = {"pair": "-DFP4Q_GEMM_CLUSTER=1", "epi16": "-DFP4Q_GEMM_EPI_WARPS=16"}
 
 
 def nvcc():
