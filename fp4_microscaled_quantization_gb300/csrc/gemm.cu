@@ -9,25 +9,41 @@
 //   E1M2 + MX                    -> kind::mxf8f6f4 on the E4M3 byte copies
 //                                   (every E1M2 level k/4 is exact in E4M3)
 //
-// Structure (persistent, 448 threads per CTA, 320 for the kernels that
-// quantize their output; a single CTA per 128 x 256 output tile, or two CTAs
-// per 256 x 256 tile, see the kernel):
-//   warp 0      TMA producer: A/B tiles (128-byte swizzled K-major rows) by
-//               cp.async.bulk.tensor and the compact 512-byte scale chunks by
-//               cp.async.bulk, into a ring of stages guarded by mbarriers.
-//   warp 1      owns the TMEM allocation; one lane issues the MMAs of a stage
-//               once its operands and scales are in place, and tcgen05.commit
-//               frees the stage.
-//   warps 2-5   epilogue: TMEM -> registers (tcgen05.ld), alpha, bf16/fp32,
-//   (+ 10-13)   then a swizzled shared-memory box stored by TMA
-//               (cp.async.bulk.tensor, bulk groups).  The accumulator is
-//               released before the stores so the next tile's MMAs overlap
-//               them.  The plain kernels drain it with eight warps, two per
-//               TMEM lane quarter (columns 0-127 and 128-255), which halves
-//               the time the next tile's MMAs wait for it.
-//   warps 6-9   scale writers, one per TMEM lane quarter: per stage they read
-//               the compact chunks from shared memory and write them to TMEM
-//               with tcgen05.st, then signal the MMA lane.
+// Structure.  Persistent clusters of two CTAs on two SMs (a cta_group::2
+// pair) own 256 x 256 output tiles; CTA r of a pair holds accumulator rows
+// 128r..128r+127 of each tile in its TMEM, loads those rows of A and rows
+// 128r..128r+127 of B, and the pair's MMAs, issued by rank 0 (the leader),
+// read both CTAs' shared memory.  Each SM so pulls 32 KB of operands per
+// K-tile of 256 out of L2 for 128 x 256 x 256 of MMA work, which L2 sustains;
+// a lone CTA on the same tile width would need 48 KB.  Roles (per CTA):
+//   warp 0      producer: A rows and this CTA's half of B by
+//               cp.async.bulk.tensor (.cta_group::2, 128-byte swizzled
+//               K-major rows) into a ring of kStages slots, the bytes
+//               completing on the leader's full barrier of the slot; and the
+//               stage's scale chunks (below).
+//   warp 1      owns the TMEM allocation (cta_group::2); on the leader one
+//               lane waits for a stage (one barrier: both CTAs' operands and
+//               both CTAs' scale writers), issues its MMAs back to back and
+//               frees the stage with one tcgen05.commit (multicast to both
+//               CTAs).  The tensor pipe queues only about one MMA ahead of
+//               the lane, so the lane does nothing else between stages.
+//   warps 6-9   scale writers, one per TMEM lane quarter.  The producer
+//               loads a stage's compact 512-byte scale chunks into the slot
+//               with its operands (cp.async.bulk, completing on a barrier of
+//               this CTA); every writer copies its rows of the chunks into the
+//               stage's TMEM scale slot with tcgen05.st and arrives on the
+//               stage's barrier in the leader.
+//   epilogue    (warps 2-5 and 10-13; 2-5 when the kernel quantizes its
+//               output) TMEM -> registers (tcgen05.ld), alpha, fp32 / bf16,
+//               the accumulator is released to the next tile's MMAs, then
+//               the stores: straight from registers to global memory in the
+//               plain kernels; through a swizzled shared-memory slice (TMA
+//               store, then the row-wise quantization of the slice) in the
+//               kernels that quantize their output.
+// Signals between the two CTAs are relaxed cluster-scope mbarrier arrivals:
+// what they announce is already complete when they are sent (TMEM writes
+// waited for with tcgen05.wait::st, TMEM reads with tcgen05.wait::ld), and a
+// release arrival would stall the sending warp for ~1000 cycles each time.
 //
 // Scale factors in TMEM.  Sub-partition q of the tensor core (accumulator
 // rows 32q..32q+31) reads its scales from TMEM lane quarter q: for A, row
@@ -37,13 +53,11 @@
 // 32-bit cell each, so lane i of every quarter stores row i of two chunks as
 // 8 consecutive columns: for B the two row groups of one K chunk (columns
 // sfb + 0..7), for A two consecutive K chunks (chunk c at sfa + 4c + 0..3, of
-// which quarter q reads cell q).  Writing the scales from registers keeps the
-// tensor pipe free of scale copies (tcgen05.cp), which cost it 15-60 cycles
-// each, and needs no shared-memory staging.
+// which quarter q reads cell q).
 //
 // Grouped launches (fp4q_gemm_group) run the same kernel over the tiles of
-// several GEMMs of one recipe, each CTA walking its own host-made tile list
-// (longest tiles first, each to the least-loaded CTA), so that GEMMs with
+// several GEMMs of one recipe, each pair walking its own host-made tile list
+// (longest tiles first, each to the least-loaded pair), so that GEMMs with
 // different K keep every SM busy to the end of one launch.
 //
 // Every mbarrier wait is bounded (about 2 s of %globaltimer); on expiry the
@@ -66,61 +80,60 @@ namespace fp4q {
 namespace {
 
 enum { KIND_MXF4 = 0, KIND_NVF4 = 1, KIND_F8 = 2 };
-// CTA cooperation: none, or a cta_group::2 pair
-enum { CL_SINGLE = 0, CL_PAIR = 1 };
 
 constexpr int BM = 128;              // accumulator rows per CTA (TMEM lanes)
 constexpr int BN = 256;              // tile columns (MMA N)
+constexpr int TM = 256;              // tile rows (the pair's two CTAs)
 constexpr int KROW = 128;            // bytes of one operand row per K-tile (one 128B swizzle span)
-constexpr int A_BYTES = BM * KROW;   // 16 KB
+constexpr int A_BYTES = BM * KROW;   // 16 KB: this CTA's rows of A
+constexpr int B_BYTES = 128 * KROW;  // 16 KB: this CTA's half of B
+constexpr int OP_STAGE = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t ACC_COL = 0;      // accumulator columns [0, 256); scale columns after it
+constexpr uint32_t ACC_COL = 0;      // accumulator columns [0, 256); scale slots after it
+constexpr int kSmemMax = 232448;     // dynamic shared memory per CTA
+constexpr int kBarBytes = 512;       // barriers, TMEM address, abort flag
 
-// Epilogue warps of the plain kernels: 8 (two per TMEM lane quarter) or 16 (four).
-#ifndef FP4Q_GEMM_EPI_WARPS
-#define FP4Q_GEMM_EPI_WARPS 8
-#endif
-static_assert(FP4Q_GEMM_EPI_WARPS == 8 || FP4Q_GEMM_EPI_WARPS == 16, "FP4Q_GEMM_EPI_WARPS");
-constexpr int kPlainBoxBytes = FP4Q_GEMM_EPI_WARPS == 16 ? 32 : 64;   // staging box row of a plain epilogue warp
-
-template <int KIND, bool PAIR, bool FUSED = false>
+template <int KIND, bool FUSED = false>
 struct KindK {
   // chunks = 512-byte groups of 4 consecutive scale bytes of one 128-row group
   static constexpr int kChunks = KIND == KIND_MXF4 ? 2 : (KIND == KIND_NVF4 ? 4 : 1);   // per K-tile
   static constexpr int kElemsPerTile = KIND == KIND_F8 ? 128 : 256;
   static constexpr int kMmaK = KIND == KIND_F8 ? 32 : 64;
   static constexpr int kBlock = KIND == KIND_NVF4 ? 16 : 32;
-  // B rows this CTA loads per tile: all 256, or its half of the pair's 256
-  static constexpr int kBRows = PAIR ? 128 : 256;
-  static constexpr int kBBytes = kBRows * KROW;
-  // compact chunks in a stage: A (kChunks), B row group 0 (kChunks), B row group 1 (kChunks)
-  static constexpr int kCompact = 3 * kChunks * 512;
-  // TMEM scale columns per stage: A 8 per two chunks (F8: 4 for its one chunk), B 8 per chunk
-  static constexpr int kSfColsA = KIND == KIND_F8 ? 4 : 4 * kChunks;
+  // one stage's compact chunks: A (kChunks), B row group 0 (kChunks), B row
+  // group 1 (kChunks), loaded with the stage's operands into its slot
+  static constexpr int kSfBytes = 3 * kChunks * 512;
+  static constexpr int kSlot = OP_STAGE + (kSfBytes + 1023) / 1024 * 1024;
+  // TMEM scale columns of a stage: A 4 per chunk, B 8 per chunk; a slot is
+  // written with one x32 store (MXF4), x32 + x16 (NVF4) or one x16 (F8)
+  static constexpr int kSfColsA = 4 * kChunks;
   static constexpr int kSfColsB = 8 * kChunks;
-  // columns per stage, padded so that one scale writer stores a stage with one
-  // (two for NV) 32x32b.x32 store, or one x16 for F8
-  static constexpr int kSfCols = KIND == KIND_MXF4 ? 32 : (KIND == KIND_NVF4 ? 64 : 16);
-  static constexpr int kStage = (A_BYTES + kBBytes + kCompact + 1023) / 1024 * 1024;
-  // threads: producer, MMA, scale-writer warps and the epilogue warps (4,
-  // or 8 / 16 when two / four drain each TMEM lane quarter)
-  static constexpr int kEpiWarps = FUSED ? 4 : FP4Q_GEMM_EPI_WARPS;
+  static constexpr int kSfCols = KIND == KIND_MXF4 ? 32 : (KIND == KIND_NVF4 ? 48 : 16);
+  // every stage has its TMEM scale slot beside the accumulator
+  static constexpr int kStagesTmem = (int)(TMEM_COLS - 256) / kSfCols;
+  // threads: producer, MMA, scale-writer warps and the epilogue warps (8, two
+  // per TMEM lane quarter; 4 in the kernels that quantize their output)
+  static constexpr int kEpiWarps = FUSED ? 4 : 8;
   static constexpr int kThreads = 32 * (6 + kEpiWarps);
   static constexpr int kEpiCols = 256 / (kEpiWarps / 4);   // accumulator columns per epilogue warp
-  // epilogue staging per warp: one 32-row store box of kBoxBytes-byte rows, or
-  // (fused output quantization) the warp's whole 32 x 256 bf16 slice of the tile
-  static constexpr int kBoxBytes = FUSED ? 128 : kPlainBoxBytes;
+  // shared-memory staging of an epilogue warp: one 32-row x 32-byte store box
+  // (plain kernels), or the warp's whole 32 x 256 bf16 slice of the tile
+  // (fused output quantization)
+  static constexpr int kBoxBytes = FUSED ? 128 : 32;
   static constexpr int kStgWarp = FUSED ? 16384 : 32 * kBoxBytes;
-  static constexpr int kStagesMax = (232448 - 1280 - kEpiWarps * kStgWarp) / kStage;
-  static constexpr int kStagesCap = kStagesMax > 6 ? 6 : kStagesMax;
-  static constexpr int kStagesTmem = (int)(TMEM_COLS - BN) / kSfCols;   // stages whose scales fit beside the accumulator
-  static constexpr int kStages = kStagesCap > kStagesTmem ? kStagesTmem : kStagesCap;
-  static constexpr int kBarOff = kStages * kStage + kEpiWarps * kStgWarp;   // stages, then the epilogue staging
-  static constexpr int kSmem = kBarOff + 256 + 1024;                 // + barriers + alignment slack
-  static_assert(kStages >= (FUSED ? 2 : 3), "pipeline depth");
-  static_assert(kSmem <= 232448, "shared memory");
+  static constexpr int kFixed = kEpiWarps * kStgWarp + kBarBytes + 1024;
+  static constexpr int kStagesFit = (kSmemMax - kFixed) / kSlot;
+  static constexpr int kStagesCap = kStagesFit > kStagesTmem ? kStagesTmem : kStagesFit;
+  static constexpr int kStages = kStagesCap > 8 ? 8 : kStagesCap;
+  static constexpr int kStgOff = kStages * kSlot;
+  static constexpr int kBarOff = kStgOff + kEpiWarps * kStgWarp;
+  static constexpr int kSmem = kBarOff + kBarBytes + 1024;   // + alignment slack
+  static_assert(kStages >= 3, "pipeline depth");
+  static_assert(kSmem <= kSmemMax, "shared memory");
   static_assert(kSfColsA + kSfColsB <= kSfCols, "scale columns");
   static_assert(ACC_COL + BN + kStages * kSfCols <= TMEM_COLS, "tensor memory");
+  static_assert((3 * kStages + 3) * 8 + 24 <= kBarBytes, "barrier area");
+  static_assert(kSlot % 1024 == 0, "slots stay aligned for the 128-byte swizzle");
 };
 
 struct GemmParams {
@@ -129,8 +142,8 @@ struct GemmParams {
   const float* ts_a;      // NV tensor scales (or null)
   const float* ts_b;
   uint32_t* status;
-  int32_t M, N, K;
   int32_t want_bf16, want_f32;
+  int32_t M, N, K;
   // fused output quantization (the kernels with QG >= 0): the row-wise copy of
   // bf16(D) as fp4q_rht_quantize would make it from the stored bf16 D
   uint8_t* q_codes;       // M x N/2
@@ -142,24 +155,24 @@ struct GemmParams {
   uint32_t q_sgn[32];     // sign words of a 32-element chunk (bit 31 = negate)
 };
 
-// Several GEMMs of one kind in one persistent launch (the plain single-CTA
-// kernels only): each CTA walks its own list of global tile ids, made on the
-// host so that the CTAs' summed tile costs are balanced (tiles of a long-K
-// GEMM cost more).  Passed by value as one kernel parameter.
+// Several GEMMs of one kind in one persistent launch (the plain kernels
+// only): each pair walks its own list of global tile ids, made on the host so
+// that the pairs' summed tile costs are balanced (tiles of a long-K GEMM cost
+// more).  Passed by value as one kernel parameter.
 constexpr int kGroupMax = 4;          // GEMMs per launch
-constexpr int kGroupMaxUnits = 256;   // CTAs
-constexpr int kGroupMaxTiles = 8192;  // tiles of all the GEMMs together
+constexpr int kGroupMaxUnits = 256;   // pairs
+constexpr int kGroupMaxTiles = 8192;  // 256 x 256 tiles of all the GEMMs together
 struct GroupArgs {
   CUtensorMap a[kGroupMax], b[kGroupMax], dh[kGroupMax], df[kGroupMax];
   const uint8_t* sfa[kGroupMax];
   const uint8_t* sfb[kGroupMax];
   const float* ts_a[kGroupMax];
   const float* ts_b[kGroupMax];
-  int32_t M[kGroupMax], N[kGroupMax], K[kGroupMax];
   int32_t want_bf16[kGroupMax], want_f32[kGroupMax];
+  int32_t M[kGroupMax], N[kGroupMax], K[kGroupMax];
   int32_t tile0[kGroupMax + 1];       // first global tile id of each GEMM; tile0[np] = all tiles
   int32_t np;
-  uint16_t unit_begin[kGroupMaxUnits + 1];   // CTA u walks order[unit_begin[u] .. unit_begin[u + 1])
+  uint16_t unit_begin[kGroupMaxUnits + 1];   // pair u walks order[unit_begin[u] .. unit_begin[u + 1])
   uint16_t order[kGroupMaxTiles];
 };
 struct NoGroupArgs {
@@ -179,9 +192,6 @@ __device__ __forceinline__ uint64_t globaltimer() {
 }
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
@@ -209,13 +219,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
   }
 }
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int32_t x, int32_t y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(dst), "l"(tm), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, int32_t x, int32_t y, uint32_t src) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
                ::"l"(tm), "r"(x), "r"(y), "r"(src)
@@ -237,34 +240,6 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
 }
 // K-major operand rows of 128 bytes, 128B swizzle, 8-row groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t op_desc(uint32_t saddr) { return sdesc(saddr, 16, 1024, 2); }
-
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-template <int KIND>
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
-                                       uint32_t sfb, uint32_t acc) {
-  if constexpr (KIND == KIND_MXF4) {
-    asm volatile(
-        "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p; }"
-        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
-        : "memory");
-  } else if constexpr (KIND == KIND_NVF4) {
-    asm volatile(
-        "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p; }"
-        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
-        : "memory");
-  } else {
-    asm volatile(
-        "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p; }"
-        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
-        : "memory");
-  }
-}
 
 // 32 consecutive fp32 accumulator columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -319,12 +294,13 @@ __device__ __forceinline__ void st_shared16(uint32_t addr, uint4 v) {
 // Instruction descriptor of the block-scaled kinds: B scale id in bits 4-5,
 // A/B element types in 7-9 / 10-12, K-major A and B, N >> 3 in 17-22, scale
 // type in 23 (1 = E8M0, 0 = E4M3), M >> 4 in 24-28, A scale id in 29-30.
-template <int KIND, int MM>
+// The pair's MMAs have M = 256.
+template <int KIND>
 __device__ __forceinline__ uint32_t make_idesc(uint32_t sf_id) {
   constexpr uint32_t ty = KIND == KIND_F8 ? 0u : 1u;   // E4M3 (f8f6f4) or E2M1 (mxf4 kinds)
   constexpr uint32_t sfmt = KIND == KIND_NVF4 ? 0u : 1u;
   return (sf_id << 4) | (ty << 7) | (ty << 10) | ((uint32_t)(BN >> 3) << 17) | (sfmt << 23) |
-         ((uint32_t)(MM >> 4) << 24) | (sf_id << 29);
+         ((uint32_t)(TM >> 4) << 24) | (sf_id << 29);
 }
 
 // ------------------------------------------------------------ cluster helpers
@@ -342,13 +318,15 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void remote_expect_tx(uint32_t cluster_bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar),
+// Arrivals on a barrier of either CTA of the pair (a shared::cluster
+// address).  Relaxed: the data the arrival announces is complete already.
+__device__ __forceinline__ void cluster_expect_tx(uint32_t cluster_bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar),
                "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+__device__ __forceinline__ void cluster_arrive(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 // TMA load into this CTA's shared memory that signals the pair leader's mbarrier.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* tm, int32_t x, int32_t y,
@@ -360,7 +338,7 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 // Commit of the pair's tensor-core work, arriving on the barrier at this
-// offset in both CTAs.
+// offset in both CTAs (an mbarrier arrival, not a data transfer).
 __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
@@ -390,55 +368,48 @@ __device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, 
         : "memory");
   }
 }
-
 // ------------------------------------------------------------ the kernel
-// Persistent.  Single CTA (PAIR = false): CTA b owns the 128 x 256 tiles b,
-// b + G, b + 2G, ... (G = gridDim.x).  CTA pair (PAIR = true, clusters of
-// two): pair c owns the 256 x 256 tiles c, c + G/2, ...; cluster rank r holds
-// accumulator rows 128r..128r+127 of each, loads those rows of A and rows
-// 128r..128r+127 of the tile's B, and tcgen05.mma.cta_group::2 issued by rank
-// 0 (the leader) reads both CTAs' operands, so each SM moves 32 KB of A/B per
-// K-tile instead of 48 KB and its tensor core reads half of B from the peer.
-// Tile id -> (m block = id / n_blocks, n block = id % n_blocks).
-// GROUP: the GEMMs of `ga` instead of the one of (tmA, tmB, tmDh, tmDf, p);
-// p then only supplies the status word.
-template <int KIND, int CL, int QG = -1, int QR = FP4Q_RTNE, bool GROUP = false>
-__global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThreads, 1)
+// Persistent clusters of two CTAs: pair c owns the 256 x 256 tiles c,
+// c + G/2, ... (G = gridDim.x), tile id -> (m block = id / n_blocks,
+// n block = id % n_blocks); or, for GROUP, the tiles of its list in `ga`
+// (p then only supplies the status word).  QG >= 0: the kernel quantizes
+// its bf16 output with grid QG and rounding QR instead of storing it plain.
+template <int KIND, int QG = -1, int QR = FP4Q_RTNE, bool GROUP = false>
+__global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
     bs_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmDh, const __grid_constant__ CUtensorMap tmDf,
                    const GemmParams p, const __grid_constant__ GroupArg<GROUP> ga) {
-  static_assert(!GROUP || (CL == CL_SINGLE && QG < 0), "grouped launches use the plain single-CTA kernel");
-  constexpr bool PAIR = CL == CL_PAIR, CLU = CL != CL_SINGLE;
-  using KK = KindK<KIND, PAIR, (QG >= 0)>;
+  static_assert(!GROUP || QG < 0, "grouped launches use the plain kernel");
+  constexpr bool FUSED = QG >= 0;
+  using KK = KindK<KIND, FUSED>;
   constexpr int S = KK::kStages;
-  constexpr int TM = CLU ? 256 : BM;                          // tile rows
-  constexpr int MMA_M = PAIR ? 256 : BM;                      // rows of one MMA (both CTAs' in a pair)
-  constexpr int SFA_OFF = A_BYTES + KK::kBBytes;              // compact chunks: A, B group 0, B group 1
-  constexpr uint32_t SF_COLS = KK::kSfCols;                   // per stage
+  constexpr int SLOT = KK::kSlot;
+  constexpr uint32_t SF_COLS = KK::kSfCols;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t stg_base = sbase + S * KK::kStage;
-  const uint32_t bar_full = sbase + KK::kBarOff;       // S: A/B of the stage landed (leader: both CTAs')
-  const uint32_t bar_empty = bar_full + 8 * S;         // S: the stage's MMAs finished
-  const uint32_t bar_sfd = bar_empty + 8 * S;          // S: this CTA's compact scale chunks landed
-  const uint32_t bar_sf = bar_sfd + 8 * S;             // S: scales in TMEM (leader: both CTAs')
-  const uint32_t bar_acc_full = bar_sf + 8 * S;
+  const uint32_t stg_base = sbase + KK::kStgOff;    // epilogue staging
+  // S (leader): a stage's operands (both CTAs) and scales (both CTAs' writers) are in place
+  const uint32_t bar_full = sbase + KK::kBarOff;
+  const uint32_t bar_empty = bar_full + 8 * S;      // S: the stage's MMAs finished (operand and scale slots free)
+  const uint32_t bar_sfd = bar_empty + 8 * S;       // S: this CTA's scale chunks of a stage landed
+  const uint32_t bar_acc_full = bar_sfd + 8 * S;
   const uint32_t bar_acc_empty = bar_acc_full + 8;
   const uint32_t bar_drain = bar_acc_empty + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + KK::kBarOff + 32 * S + 24);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + KK::kBarOff + 32 * S + 32);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + (bar_drain + 8 - sbase));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + (bar_drain + 16 - sbase));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = CLU ? cluster_rank() : 0u;
-  const bool leader = !PAIR || rank == 0;                              // issues MMAs
-  const int unit = CLU ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;     // cluster or CTA index
-  const int n_units = CLU ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;                   // issues MMAs
+  const int unit = (int)(blockIdx.x >> 1);         // pair index
+  const int n_units = (int)(gridDim.x >> 1);
   const int n_blocks = (p.N + BN - 1) / BN;
   const int n_tiles = ((p.M + TM - 1) / TM) * n_blocks;
 
-  // The tiles this CTA walks, by work index w in [w_begin, w_end) step w_step,
-  // and what a tile needs: its GEMM (gi), corner, shape and K-tile count.
+  // The tiles this pair walks, by work index w in [w_begin, w_end) step
+  // w_step, and what a tile needs: its GEMM (gi), this CTA's corner, shape
+  // and K-tile count.
   struct TileCtx {
     int gi, m0, n0, M, N, K, num_kt, nq;
   };
@@ -490,54 +461,36 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
     if constexpr (GROUP) return &ga.df[gi];
     else return &tmDf;
   };
-  auto sfa_of = [&](int gi) -> const uint8_t* {
-    if constexpr (GROUP) return ga.sfa[gi];
-    else return p.sfa;
-  };
-  auto sfb_of = [&](int gi) -> const uint8_t* {
-    if constexpr (GROUP) return ga.sfb[gi];
-    else return p.sfb;
-  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(bar_full + 8 * s, PAIR ? 2 : 1);   // one expect_tx arrival per producer
-      mbar_init(bar_empty + 8 * s, 1);            // the (leader's) commit
-      mbar_init(bar_sfd + 8 * s, 1);
-      mbar_init(bar_sf + 8 * s, PAIR ? 8 : 4);     // one arrival per scale-writer warp
+      mbar_init(bar_full + 8 * s, 10);     // both producers' expect_tx and the 8 scale-writer warps
+      mbar_init(bar_empty + 8 * s, 1);     // the leader's commit
+      mbar_init(bar_sfd + 8 * s, 1);       // this CTA's producer
     }
     mbar_init(bar_acc_full, 1);
-    mbar_init(bar_acc_empty, (PAIR ? 2 : 1) * KK::kEpiWarps);   // one arrival per epilogue warp
+    mbar_init(bar_acc_empty, 2 * KK::kEpiWarps);   // one arrival per epilogue warp of both CTAs
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
-    if constexpr (PAIR) {
-      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                   "r"(TMEM_COLS)
-                   : "memory");
-      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-    } else {
-      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                   "r"(TMEM_COLS)
-                   : "memory");
-      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  if constexpr (CLU) cluster_sync();
-  else __syncthreads();
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // barriers the leader owns, as seen from this CTA
-  const uint32_t lead_full = PAIR ? mapa(bar_full, 0) : bar_full;
-  const uint32_t lead_sf = PAIR ? mapa(bar_sf, 0) : bar_sf;
-  const uint32_t lead_acc_empty = PAIR ? mapa(bar_acc_empty, 0) : bar_acc_empty;
+  const uint32_t lead_full = mapa(bar_full, 0);
+  const uint32_t lead_acc_empty = mapa(bar_acc_empty, 0);
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- producer
+      // ---------------- operand producer
       if constexpr (GROUP) {
         for (int q = 0; q < ga.np; ++q) {
           asm volatile("prefetch.tensormap [%0];" ::"l"(&ga.a[q]) : "memory");
@@ -548,86 +501,75 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
         asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
       }
       uint32_t it = 0;
-      for (int w = w_begin; w < w_end && !*abort_flag; w += w_step) {
+      bool ok = true;
+      for (int w = w_begin; w < w_end && ok; w += w_step) {
         const TileCtx t = tile_ctx(w);
-        const int m0 = t.m0, n0 = t.n0, nq = t.nq;
-        const bool rg1 = (n0 + 128) < t.N;   // the tile's second 128-row group of B exists
-        const bool rows = m0 < t.M;          // this CTA's rows of A exist (false only for a 128-row tail)
         const CUtensorMap* mA = map_a(t.gi);
         const CUtensorMap* mB = map_b(t.gi);
-        const uint8_t* sfa_g = sfa_of(t.gi);
-        const uint8_t* sfb_g = sfb_of(t.gi);
+        const bool rows = t.m0 < t.M;          // false only for the second CTA of a 128-row tail
+        const bool rg1 = (t.n0 + 128) < t.N;   // the tile's second 128-row group of B exists
+        const uint8_t* sfa_g;
+        const uint8_t* sfb_g;
+        if constexpr (GROUP) {
+          sfa_g = ga.sfa[t.gi];
+          sfb_g = ga.sfb[t.gi];
+        } else {
+          sfa_g = p.sfa;
+          sfb_g = p.sfb;
+        }
+        const uint8_t* sfa_t = sfa_g + (size_t)(t.m0 / 128) * t.nq * 512;
+        const uint8_t* sfb_t = sfb_g + (size_t)(t.n0 / 128) * t.nq * 512;
         for (int kt = 0; kt < t.num_kt; ++kt, ++it) {
           const int s = (int)(it % S);
-          const uint32_t ph = (it / S) & 1u;
-          if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag)) {
-            *abort_flag = 1;
-            raise_status(p.status, FP4Q_DEV_TIMEOUT);
+          if (!mbar_wait(bar_empty + 8 * s, ((it / S) & 1u) ^ 1u, abort_flag)) {
+            ok = false;
             break;
           }
+          const uint32_t st = sbase + (uint32_t)s * SLOT;
+          const uint32_t fb = lead_full + 8 * s;
+          cluster_expect_tx(fb, OP_STAGE);
+          // rows past M or N (a 128-row tail) are zero-filled and still counted
+          tma_load_2d_pair(st, mA, kt * KROW, t.m0, fb);
+          tma_load_2d_pair(st + A_BYTES, mB, kt * KROW, t.n0 + 128 * (int)rank, fb);
+          // this CTA's scale chunks of the stage, for its scale writers
           const int q0 = kt * KK::kChunks;
-          const int nch = min(KK::kChunks, nq - q0);
-          const uint32_t sf_bytes = (uint32_t)nch * 512u;
-          const uint32_t st = sbase + (uint32_t)s * KK::kStage;
-          // the scale chunks complete on this CTA's own barrier: the full barrier
-          // itself for a single CTA, a separate one in a pair (whose full
-          // barrier lives in the leader)
-          const uint32_t fb = lead_full + 8 * s, sb = PAIR ? bar_sfd + 8 * s : bar_full + 8 * s;
-          const uint32_t sf_tx = sf_bytes * ((rows ? 1u : 0u) + (rg1 ? 2u : 1u));
-          if constexpr (PAIR) {
-            remote_expect_tx(fb, A_BYTES + KK::kBBytes);
-            tma_load_2d_pair(st, mA, kt * KROW, m0, fb);
-            tma_load_2d_pair(st + A_BYTES, mB, kt * KROW, n0 + 128 * (int)rank, fb);
-          } else {
-            mbar_expect_tx(fb, A_BYTES + KK::kBBytes + sf_tx);
-            tma_load_2d(st, mA, kt * KROW, m0, fb);
-            tma_load_2d(st + A_BYTES, mB, kt * KROW, n0, fb);
-          }
-          if constexpr (PAIR) mbar_expect_tx(sb, sf_tx);
-          if (rows) bulk_load(st + SFA_OFF, sfa_g + ((size_t)(m0 / 128) * nq + q0) * 512, sf_bytes, sb);
-          bulk_load(st + SFA_OFF + KK::kChunks * 512, sfb_g + ((size_t)(n0 / 128) * nq + q0) * 512, sf_bytes, sb);
-          if (rg1)
-            bulk_load(st + SFA_OFF + 2 * KK::kChunks * 512, sfb_g + ((size_t)(n0 / 128 + 1) * nq + q0) * 512,
-                      sf_bytes, sb);
+          const uint32_t sf_bytes = (uint32_t)min(KK::kChunks, t.nq - q0) * 512u;
+          const uint32_t sb = bar_sfd + 8 * s, ca = st + OP_STAGE;
+          mbar_expect_tx(sb, sf_bytes * ((rows ? 1u : 0u) + (rg1 ? 2u : 1u)));
+          if (rows) bulk_load(ca, sfa_t + (size_t)q0 * 512, sf_bytes, sb);
+          bulk_load(ca + KK::kChunks * 512, sfb_t + (size_t)q0 * 512, sf_bytes, sb);
+          if (rg1) bulk_load(ca + 2 * KK::kChunks * 512, sfb_t + ((size_t)t.nq + q0) * 512, sf_bytes, sb);
         }
       }
-      // In a cluster the peer's commits arrive on this CTA's empty barriers:
-      // wait for the last use of every slot, so that none lands after exit.
-      if constexpr (CLU) {
-        for (int i = 0; i < S && !*abort_flag; ++i, ++it) {
-          const int s = (int)(it % S);
-          if (!mbar_wait(bar_empty + 8 * s, ((it / S) & 1u) ^ 1u, abort_flag)) {
-            *abort_flag = 1;
-            raise_status(p.status, FP4Q_DEV_TIMEOUT);
-          }
-        }
+      // The leader's commits arrive on this CTA's empty barriers: wait for the
+      // last use of every slot, so that none lands after exit.
+      for (int i = 0; i < S && ok; ++i, ++it) {
+        const int s = (int)(it % S);
+        ok = mbar_wait(bar_empty + 8 * s, ((it / S) & 1u) ^ 1u, abort_flag);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        raise_status(p.status, FP4Q_DEV_TIMEOUT);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issue (lane 0 of the leader)
-    // Nothing sits between the MMAs of a stage: a barrier test between them
-    // (measured) leaves the tensor pipe idle, as each MMA is issued only about
-    // as fast as the pipe retires one.  The next stage is waited for after
-    // the commit; at a tile's end the accumulator is committed first and the
-    // next tile's first stage is waited for once the accumulator is free.
+    // Per stage one wait (operands and scales in place), the MMAs back to
+    // back and one commit: the tensor pipe queues about one MMA ahead, so
+    // any further work here between stages leaves it idle.
     if (lane == 0 && leader) {
-      uint32_t tl = 0, s = 0, ph = 0;
+      uint32_t tl = 0, it = 0;
       bool ok = true;
-      // single CTA: the scale writers arrive on bar_sf only after the stage's
-      // full barrier completed, so bar_sf alone orders the operands too
-      auto stage_ready = [&](uint32_t ss, uint32_t pp) -> bool {
-        if constexpr (PAIR) return mbar_wait(bar_full + 8 * ss, pp, abort_flag) && mbar_wait(bar_sf + 8 * ss, pp, abort_flag);
-        else return mbar_wait(bar_sf + 8 * ss, pp, abort_flag);
-      };
       for (int w = w_begin; w < w_end && ok; w += w_step, ++tl) {
         const TileCtx t = tile_ctx(w);
-        const int num_kt = t.num_kt;
-        ok = mbar_wait(bar_acc_empty, (tl & 1u) ^ 1u, abort_flag) && stage_ready(s, ph);
-        if (!ok) break;
-        for (int kt = 0; kt < num_kt; ++kt) {
+        ok = mbar_wait(bar_acc_empty, (tl & 1u) ^ 1u, abort_flag);
+        for (int kt = 0; kt < t.num_kt && ok; ++kt, ++it) {
+          const uint32_t s = it % S;
+          ok = mbar_wait(bar_full + 8 * s, (it / S) & 1u, abort_flag);
+          if (!ok) break;
           tc_fence_after();
-          const uint32_t st = sbase + s * KK::kStage;
+          const uint32_t st = sbase + s * SLOT;
           const uint32_t sfa_col = tmem + ACC_COL + BN + SF_COLS * s;
           const uint32_t sfb_col = sfa_col + KK::kSfColsA;
           const int rem = t.K - kt * KK::kElemsPerTile;
@@ -648,13 +590,8 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
               sf_id = (uint32_t)k;
             }
             const uint32_t acc = k > 0 ? 1u : acc0;
-            if constexpr (PAIR)
-              tc_mma_pair<KIND>(tmem + ACC_COL, da + 2u * k, db + 2u * k, make_idesc<KIND, MMA_M>(sf_id), sfa, sfb, acc);
-            else
-              tc_mma<KIND>(tmem + ACC_COL, da + 2u * k, db + 2u * k, make_idesc<KIND, MMA_M>(sf_id), sfa, sfb, acc);
+            tc_mma_pair<KIND>(tmem + ACC_COL, da + 2u * k, db + 2u * k, make_idesc<KIND>(sf_id), sfa, sfb, acc);
           };
-          const bool has_next = kt + 1 < num_kt;
-          const uint32_t s2 = s + 1 == (uint32_t)S ? 0u : s + 1, ph2 = s + 1 == (uint32_t)S ? ph ^ 1u : ph;
           if (n_mma == 4) {
             issue(0);
             issue(1);
@@ -663,27 +600,18 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
           } else {
             for (int k = 0; k < n_mma; ++k) issue(k);
           }
-          if constexpr (PAIR) tc_commit_pair(bar_empty + 8 * s);
-          else tc_commit(bar_empty + 8 * s);
-          if (has_next) ok = stage_ready(s2, ph2);
-          s = s2;
-          ph = ph2;
-          if (!ok) break;
+          tc_commit_pair(bar_empty + 8 * s);
         }
         if (!ok) break;
-        if constexpr (PAIR) tc_commit_pair(bar_acc_full);
-        else tc_commit(bar_acc_full);
+        tc_commit_pair(bar_acc_full);
       }
       if (!ok) {
         *abort_flag = 1;
         raise_status(p.status, FP4Q_DEV_TIMEOUT);
       }
       // wait (bounded) until every tensor-core operation this lane issued finished
-      if constexpr (PAIR)
-        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar_drain)
-                     : "memory");
-      else
-        tc_commit(bar_drain);
+      asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar_drain)
+                   : "memory");
       const uint64_t t0 = globaltimer();
       while (!mbar_try(bar_drain, 0) && globaltimer() - t0 < 2000000000ull) {
       }
@@ -691,47 +619,46 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
     __syncwarp();
   } else if (warp >= 6 && warp < 10) {
     // ---------------- scale writers: lane i of quarter q stores row i of the compact chunks
+    // A stage's chunks land in its slot once the slot's previous MMAs have
+    // finished (the producer waited for them), so the TMEM scale slot of the
+    // stage is free too, and the full barrier of the slot is in this stage's
+    // phase; one wait per stage.
     const uint32_t qbase = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     uint32_t it = 0;
     bool ok = true;
     for (int w = w_begin; w < w_end && ok; w += w_step) {
       const int num_kt = tile_ctx(w).num_kt;
       for (int kt = 0; kt < num_kt; ++kt, ++it) {
-        const int s = (int)(it % S);
-        const uint32_t ph = (it / S) & 1u;
-        ok = mbar_wait(PAIR ? bar_sfd + 8 * s : bar_full + 8 * s, ph, abort_flag);
+        const uint32_t s = it % S;
+        ok = mbar_wait(bar_sfd + 8 * s, (it / S) & 1u, abort_flag);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t st = sbase + (uint32_t)s * KK::kStage;
-        const uint32_t ca = st + SFA_OFF, cb0 = ca + KK::kChunks * 512, cb1 = cb0 + KK::kChunks * 512;
-        const uint32_t sfa_col = qbase + ACC_COL + BN + SF_COLS * (uint32_t)s;
-        const uint32_t sfb_col = sfa_col + KK::kSfColsA;
-        // the stage's columns in order: A chunks (4 each), then per B chunk its two row groups
-        uint32_t w[KK::kSfCols];
+        const uint32_t ca = sbase + s * SLOT + OP_STAGE, cb0 = ca + KK::kChunks * 512, cb1 = cb0 + KK::kChunks * 512;
+        const uint32_t sfa_col = qbase + ACC_COL + BN + SF_COLS * s;
+        // the slot's columns in order: A chunks (4 each), then per B chunk its two row groups
+        uint32_t wv[KK::kSfCols];
 #pragma unroll
-        for (int c = 0; c < KK::kChunks; ++c) put4(w + 4 * c, chunk_row(ca + 512u * c, lane));
+        for (int c = 0; c < KK::kChunks; ++c) put4(wv + 4 * c, chunk_row(ca + 512u * c, lane));
 #pragma unroll
         for (int c = 0; c < KK::kChunks; ++c) {
-          put4(w + KK::kSfColsA + 8 * c, chunk_row(cb0 + 512u * c, lane));
-          put4(w + KK::kSfColsA + 8 * c + 4, chunk_row(cb1 + 512u * c, lane));
+          put4(wv + KK::kSfColsA + 8 * c, chunk_row(cb0 + 512u * c, lane));
+          put4(wv + KK::kSfColsA + 8 * c + 4, chunk_row(cb1 + 512u * c, lane));
         }
 #pragma unroll
-        for (int j = KK::kSfColsA + KK::kSfColsB; j < KK::kSfCols; ++j) w[j] = 0u;
+        for (int c = KK::kSfColsA + KK::kSfColsB; c < KK::kSfCols; ++c) wv[c] = 0u;
         if constexpr (KK::kSfCols == 16) {
-          tmem_st16(sfa_col, w);
+          tmem_st16(sfa_col, wv);
+        } else if constexpr (KK::kSfCols == 48) {
+          tmem_st32(sfa_col, wv);
+          tmem_st16(sfa_col + 32, wv + 32);
         } else {
-#pragma unroll
-          for (int h = 0; h < KK::kSfCols / 32; ++h) tmem_st32(sfa_col + 32 * h, w + 32 * h);
+          tmem_st32(sfa_col, wv);
         }
-        (void)sfb_col;
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          if constexpr (PAIR) remote_arrive(lead_sf + 8 * s);
-          else mbar_arrive(lead_sf + 8 * s);
-        }
+        if (lane == 0) cluster_arrive(lead_full + 8 * s);
       }
     }
     if (!ok && lane == 0) {
@@ -742,25 +669,25 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
     // ---------------- epilogue (warps 2..5 and 10..13 -> TMEM lane quarters 2, 3, 0, 1)
     const int sp = warp & 3;
     const uint32_t lane_base = tmem + ((uint32_t)(32 * sp) << 16) + ACC_COL;
-    const int grp = warp < 6 ? 0 : (warp - 6) >> 2;                // warps 2-5, 10-13, 14-17, 18-21
+    const int grp = warp < 6 ? 0 : 1;                              // warps 2-5: columns 0-127, 10-13: 128-255
+    const int cbase = grp * KK::kEpiCols;                          // this warp's accumulator columns
     const int epi = grp * 4 + ((warp - 2) & 3);
     const uint32_t stg = stg_base + (uint32_t)epi * KK::kStgWarp;
-    // swizzled boxes of 32 rows: 16-byte unit u of row `lane` sits at unit
-    // u ^ (lane & 7) with 128-byte rows (fused kernels), u ^ ((lane >> 1) & 3)
-    // with 64-byte rows, u ^ ((lane >> 2) & 1) with 32-byte rows
+    // swizzled 32-row boxes: 16-byte unit u of row `lane` sits at unit
+    // u ^ (lane & 7) with 128-byte rows (fused kernels), u ^ ((lane >> 2) & 1)
+    // with 32-byte rows (plain kernels)
     constexpr uint32_t BOXB = KK::kBoxBytes;
+    static_assert(BOXB == 128 || BOXB == 32, "box row size");
     const uint32_t row_off = BOXB * (uint32_t)lane;
-    const uint32_t swz = BOXB == 128 ? (uint32_t)(lane & 7)
-                                     : (BOXB == 64 ? (uint32_t)((lane >> 1) & 3) : (uint32_t)((lane >> 2) & 1));
-    const int cbase = grp * KK::kEpiCols;                          // this warp's accumulator columns
+    const uint32_t swz = BOXB == 128 ? (uint32_t)(lane & 7) : (uint32_t)((lane >> 2) & 1);
     float alpha = 1.0f;
     if constexpr (KIND == KIND_NVF4 && !GROUP) alpha = __fmul_rn(*p.ts_a, *p.ts_b);
     uint32_t tl = 0;
     for (int w = w_begin; w < w_end; w += w_step, ++tl) {
       const TileCtx t = tile_ctx(w);
       const int m0 = t.m0, n0 = t.n0;
-      const int y = m0 + 32 * sp;
-      const bool live = m0 < t.M;   // false only for the second CTA of a 128-row tail tile
+      const int y = m0 + 32 * sp;                // first row of this warp's slice
+      const bool live = m0 < t.M;                // false only for the second CTA of a 128-row tail tile
       const CUtensorMap* mDh = map_dh(t.gi);
       const CUtensorMap* mDf = map_df(t.gi);
       bool want_bf16 = p.want_bf16, want_f32 = p.want_f32;
@@ -780,12 +707,13 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
       }
       tc_fence_after();
       const int ncols = min(BN, t.N - n0);   // 128 or 256
-      if constexpr (QG >= 0) {
+      if constexpr (FUSED) {
         // Fused output quantization.  The warp's 32 x 256 bf16 slice goes to
         // shared memory as four swizzled 32 x 64 boxes (the previous tile's
         // stores must have read them), the accumulator is released, the boxes
         // are stored by TMA when D is wanted, and each thread quantizes its
-        // row from them, 32 values at a time.
+        // row from them, 32 values at a time.  Box rows are 128 bytes: 16-byte
+        // unit u of row `lane` sits at unit u ^ (lane & 7).
         if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         __syncwarp();
 #pragma unroll
@@ -807,17 +735,15 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
             const uint32_t box = stg + 4096u * (uint32_t)(c0 / 64), u0 = 4u * (uint32_t)((c0 / 32) & 1);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              st_shared16(box + row_off + 16u * ((u0 + j) ^ swz), make_uint4(hw[4 * j], hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]));
+              st_shared16(box + row_off + 16u * ((u0 + j) ^ swz),
+                          make_uint4(hw[4 * j], hw[4 * j + 1], hw[4 * j + 2], hw[4 * j + 3]));
           }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          if constexpr (PAIR) remote_arrive(lead_acc_empty);
-          else mbar_arrive(lead_acc_empty);
-        }
+        if (lane == 0) cluster_arrive(lead_acc_empty);
         if (!live) continue;
-        if (p.want_bf16) {
+        if (want_bf16) {
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
           if (lane == 0) {
@@ -825,100 +751,95 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
           }
         }
-        if constexpr (QG >= 0) {
-          const int64_t row = (int64_t)y + lane;
-  #pragma unroll 1
-          for (int c0 = 0; c0 < ncols; c0 += 32) {
-            const uint32_t box = stg + 4096u * (uint32_t)(c0 / 64), u0 = 4u * (uint32_t)((c0 / 32) & 1);
-            uint32_t w[16];
-  #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint4 v = chunk_row(box + row_off + 16u * ((u0 + j) ^ swz), 0);
-              w[4 * j] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
+        const int64_t row = (int64_t)y + lane;
+#pragma unroll 1
+        for (int c0 = 0; c0 < ncols; c0 += 32) {
+          const uint32_t box = stg + 4096u * (uint32_t)(c0 / 64), u0 = 4u * (uint32_t)((c0 / 32) & 1);
+          uint32_t wq[16];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) put4(wq + 4 * j, chunk_row(box + row_off + 16u * ((u0 + j) ^ swz), 0));
+          float2 P[16];
+          chunk_from_bf16_words(wq, p.q_sgn, P);
+          // MX output scales: H16's 1/4 goes into the power-of-two block scale
+          if (p.q_nh == 16) rotate_chunk<16, false>(P);
+          else if (p.q_nh == 32) rotate_chunk<32>(P);
+          ChunkOut o;
+          const int64_t col = (int64_t)n0 + c0;
+          quantize_chunk<(QG >= 0 ? QG : 0), FP4Q_SCALE_MX, QR>(P, 0.0f, (uint64_t)(row * p.N + col), 0u, p.q_keys,
+                                                                 p.q_e4m3 != nullptr, p.status, o,
+                                                                 p.q_nh == 16 ? 2 : 0);
+          *reinterpret_cast<uint4*>(p.q_codes + row * (p.N / 2) + col / 2) = make_uint4(o.w[0], o.w[1], o.w[2], o.w[3]);
+          const int64_t nkb = p.N / 32, k = col / 32;
+          p.q_scales[p.q_sf_mma ? sf_mma_offset(row, k, nkb) : row * nkb + k] = (uint8_t)o.sbytes;
+          if (p.q_e4m3) {
+            uint4* ep = reinterpret_cast<uint4*>(p.q_e4m3 + row * p.N + col);
+            ep[0] = make_uint4(o.e4[0], o.e4[1], o.e4[2], o.e4[3]);
+            ep[1] = make_uint4(o.e4[4], o.e4[5], o.e4[6], o.e4[7]);
+          }
+        }
+      } else {
+        // Plain output through a 32-row x 32-byte swizzled box per warp, stored
+        // by TMA: fp32 columns as they leave TMEM, the bf16 row slice once the
+        // accumulator is released.
+        constexpr int ECOLS = KK::kEpiCols, UNITS = (int)BOXB / 16;   // 16-byte units per box row
+        constexpr int FCOLS = (int)BOXB / 4, HCOLS = (int)BOXB / 2;   // columns of an fp32 / bf16 box
+        uint32_t h[ECOLS / 2];   // this warp's columns of the row as packed bf16
+#pragma unroll
+        for (int c0 = 0; c0 < ECOLS; c0 += 32) {
+          if (cbase + c0 < ncols) {
+            uint32_t r[32];
+            tmem_ld32(lane_base + (uint32_t)(cbase + c0), r);
+            if constexpr (KIND == KIND_NVF4) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), alpha));
             }
-            float2 P[16];
-            chunk_from_bf16_words(w, p.q_sgn, P);
-            // MX output scales: H16's 1/4 goes into the power-of-two block scale
-            if (p.q_nh == 16) rotate_chunk<16, false>(P);
-            else if (p.q_nh == 32) rotate_chunk<32>(P);
-            ChunkOut o;
-            const int64_t col = (int64_t)n0 + c0;
-            quantize_chunk<QG, FP4Q_SCALE_MX, QR>(P, 0.0f, (uint64_t)(row * p.N + col), 0u, p.q_keys,
-                                                  p.q_e4m3 != nullptr, p.status, o, p.q_nh == 16 ? 2 : 0);
-            *reinterpret_cast<uint4*>(p.q_codes + row * (p.N / 2) + col / 2) = make_uint4(o.w[0], o.w[1], o.w[2], o.w[3]);
-            const int64_t nkb = p.N / 32, k = col / 32;
-            p.q_scales[p.q_sf_mma ? sf_mma_offset(row, k, nkb) : row * nkb + k] = (uint8_t)o.sbytes;
-            if (p.q_e4m3) {
-              uint4* ep = reinterpret_cast<uint4*>(p.q_e4m3 + row * p.N + col);
-              ep[0] = make_uint4(o.e4[0], o.e4[1], o.e4[2], o.e4[3]);
-              ep[1] = make_uint4(o.e4[4], o.e4[5], o.e4[6], o.e4[7]);
+            if (want_f32 && live) {
+#pragma unroll
+              for (int hh = 0; hh < 32 / FCOLS; ++hh) {
+                if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                __syncwarp();
+#pragma unroll
+                for (int u = 0; u < UNITS; ++u)
+                  st_shared16(stg + row_off + 16u * ((uint32_t)u ^ swz),
+                              make_uint4(r[FCOLS * hh + 4 * u], r[FCOLS * hh + 4 * u + 1], r[FCOLS * hh + 4 * u + 2],
+                                         r[FCOLS * hh + 4 * u + 3]));
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                  tma_store_2d(mDf, n0 + cbase + c0 + FCOLS * hh, y, stg);
+                  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                }
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const __nv_bfloat162 b2 =
+                  __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+              h[c0 / 2 + j] = *reinterpret_cast<const uint32_t*>(&b2);
             }
           }
         }
-        continue;
-      }
-      constexpr int ECOLS = KK::kEpiCols, UNITS = (int)BOXB / 16;   // 16-byte units per box row
-      constexpr int FCOLS = (int)BOXB / 4, HCOLS = (int)BOXB / 2;   // columns of an fp32 / bf16 box
-      uint32_t h[ECOLS / 2];   // this warp's columns of the row as packed bf16
+        // accumulator consumed: let the next tile's MMAs start
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) cluster_arrive(lead_acc_empty);
+        if (want_bf16 && live) {
 #pragma unroll
-      for (int c0 = 0; c0 < ECOLS; c0 += 32) {
-        if (cbase + c0 < ncols) {
-          uint32_t r[32];
-          tmem_ld32(lane_base + (uint32_t)(cbase + c0), r);
-          if constexpr (KIND == KIND_NVF4) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), alpha));
-          }
-          if (want_f32 && live) {
-            // 32-row x FCOLS-float boxes
-#pragma unroll
-            for (int hh = 0; hh < 32 / FCOLS; ++hh) {
+          for (int b = 0; b < ECOLS / HCOLS; ++b) {
+            if (cbase + HCOLS * b < ncols) {
               if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
               __syncwarp();
 #pragma unroll
               for (int u = 0; u < UNITS; ++u)
                 st_shared16(stg + row_off + 16u * ((uint32_t)u ^ swz),
-                            make_uint4(r[FCOLS * hh + 4 * u], r[FCOLS * hh + 4 * u + 1], r[FCOLS * hh + 4 * u + 2],
-                                       r[FCOLS * hh + 4 * u + 3]));
+                            make_uint4(h[(HCOLS / 2) * b + 4 * u], h[(HCOLS / 2) * b + 4 * u + 1],
+                                       h[(HCOLS / 2) * b + 4 * u + 2], h[(HCOLS / 2) * b + 4 * u + 3]));
               asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
               __syncwarp();
               if (lane == 0) {
-                tma_store_2d(mDf, n0 + cbase + c0 + FCOLS * hh, y, stg);
+                tma_store_2d(mDh, n0 + cbase + HCOLS * b, y, stg);
                 asm volatile("cp.async.bulk.commit_group;" ::: "memory");
               }
-            }
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-            h[c0 / 2 + j] = *reinterpret_cast<const uint32_t*>(&b2);
-          }
-        }
-      }
-      // accumulator consumed: let the next tile's MMAs start
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (PAIR) remote_arrive(lead_acc_empty);
-        else mbar_arrive(lead_acc_empty);
-      }
-      if (want_bf16 && live) {
-        // 32-row x HCOLS-bf16 boxes
-#pragma unroll
-        for (int b = 0; b < ECOLS / HCOLS; ++b) {
-          if (cbase + HCOLS * b < ncols) {
-            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-            __syncwarp();
-#pragma unroll
-            for (int u = 0; u < UNITS; ++u)
-              st_shared16(stg + row_off + 16u * ((uint32_t)u ^ swz),
-                          make_uint4(h[(HCOLS / 2) * b + 4 * u], h[(HCOLS / 2) * b + 4 * u + 1],
-                                     h[(HCOLS / 2) * b + 4 * u + 2], h[(HCOLS / 2) * b + 4 * u + 3]));
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(mDh, n0 + cbase + HCOLS * b, y, stg);
-              asm volatile("cp.async.bulk.commit_group;" ::: "memory");
             }
           }
         }
@@ -928,116 +849,98 @@ __global__ void __launch_bounds__(KindK<KIND, CL == CL_PAIR, (QG >= 0)>::kThread
     __syncwarp();
   }
   tc_fence_before();
-  // no CTA of a cluster may leave while its peer can still use its shared or tensor memory
-  if constexpr (CLU) cluster_sync();
-  else __syncthreads();
+  // no CTA of a pair may leave while its peer can still use its shared or tensor memory
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    if constexpr (PAIR)
-      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
-    else
-      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
   }
 }
 
 // ------------------------------------------------------------ host side
-// 2-D byte tensor [rows][row_bytes], box = 128 bytes x box_rows, 128B swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
-  return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, (uint32_t)KROW,
-                        box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+// 2-D byte tensor [rows][row_bytes], box = 128 bytes x 128 rows, 128B swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows) {
+  return encode_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, row_bytes, rows, row_bytes, (uint32_t)KROW, 128u,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
 }
 // Output [M][N] of bf16 or fp32, boxes of 32 rows x box_bytes with the
-// swizzle of that row size (32 or 64 bytes for the plain kernels, 128 for the
-// fused ones).
+// swizzle of that row size (32 bytes for the plain kernels, 128 for the fused
+// ones); the kernels' staging uses the same box.
 bool make_out_map(CUtensorMap* m, const void* base, uint64_t N, uint64_t M, bool f32, uint32_t box_bytes) {
   return encode_tmap_2d(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, N, M,
                         N * (f32 ? 4u : 2u), box_bytes / (f32 ? 4u : 2u), 32u,
-                        box_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
-                                        : (box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B));
+                        box_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B);
 }
+constexpr uint32_t kPlainBox = KindK<KIND_MXF4, false>::kBoxBytes;
+constexpr uint32_t kFusedBox = KindK<KIND_MXF4, true>::kBoxBytes;
+static_assert(kPlainBox == 32 && kFusedBox == 128, "output maps");
 
-template <int KIND, int CL, int QG = -1, int QR = FP4Q_RTNE>
-cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& dh, const CUtensorMap& df,
-                        const GemmParams& p, cudaStream_t s) {
-  constexpr bool CLU = CL != CL_SINGLE;
-  using KK = KindK<KIND, CL == CL_PAIR, (QG >= 0)>;
-  static unsigned attr_set = 0;   // one bit per device ordinal < 32
+// Opt a kernel into its dynamic shared memory and find how many pairs can be
+// resident at once, once per device (cached).  Returns 0 on error.
+template <class Kern>
+int resident_pairs(Kern kern, int smem, int threads, unsigned& done, int (&max_pairs)[32]) {
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   const unsigned bit = dev < 32 ? (1u << dev) : 0u;
-  if (!(attr_set & bit) || !bit) {
-    e = cudaFuncSetAttribute(bs_gemm_kernel<KIND, CL, QG, QR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             KK::kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set |= bit;
-  }
-  const int tm = CLU ? 256 : BM;
-  const int tiles = ((p.M + tm - 1) / tm) * ((p.N + BN - 1) / BN);
+  if (bit && (done & bit)) return max_pairs[dev];
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(KK::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = KK::kSmem;
-  cfg.stream = s;
+  cfg.gridDim = dim3((unsigned)num_sms() & ~1u, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CLU ? 2 : 1;
+  attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = CLU ? 1 : 0;
-  int units = num_sms();
-  if constexpr (CLU) {
-    // persistent clusters: no more than can be resident at once (a GPC with an
-    // odd number of free SMs leaves one out)
-    static int max_clusters[32] = {};
-    if (!bit || max_clusters[dev] == 0) {
-      cfg.gridDim = dim3((unsigned)num_sms() & ~1u, 1, 1);
-      int n = 0;
-      e = cudaOccupancyMaxActiveClusters(&n, bs_gemm_kernel<KIND, CL, QG, QR>, &cfg);
-      if (e != cudaSuccess) return e;
-      if (n <= 0) return cudaErrorInvalidConfiguration;
-      if (bit) max_clusters[dev] = n;
-      units = n;
-    } else {
-      units = max_clusters[dev];
-    }
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) return 0;
+  if (bit) {
+    max_pairs[dev] = n;
+    done |= bit;
   }
-  if (tiles < units) units = tiles;
-  cfg.gridDim = dim3((unsigned)(CLU ? 2 * units : units), 1, 1);
-  return cudaLaunchKernelEx(&cfg, bs_gemm_kernel<KIND, CL, QG, QR>, a, b, dh, df, p, NoGroupArgs{});
+  return n;
 }
 
-// One launch over the GEMMs of ga (plain single-CTA kernel); grid = the units
-// of ga's schedule.  p supplies the status word only.
-template <int KIND>
-cudaError_t launch_gemm_group(const GroupArgs& ga, int units, const GemmParams& p, cudaStream_t s) {
-  using KK = KindK<KIND, false, false>;
-  static unsigned attr_set = 0;   // one bit per device ordinal < 32
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const unsigned bit = dev < 32 ? (1u << dev) : 0u;
-  if (!(attr_set & bit) || !bit) {
-    e = cudaFuncSetAttribute(bs_gemm_kernel<KIND, CL_SINGLE, -1, FP4Q_RTNE, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, KK::kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set |= bit;
-  }
+template <class Kern, class... Args>
+cudaError_t launch_pairs(Kern kern, int pairs, int smem, int threads, cudaStream_t s, Args... args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)units, 1, 1);
-  cfg.blockDim = dim3(KK::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = KK::kSmem;
+  cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = s;
-  return cudaLaunchKernelEx(&cfg, bs_gemm_kernel<KIND, CL_SINGLE, -1, FP4Q_RTNE, true>, ga.a[0], ga.b[0], ga.dh[0],
-                            ga.df[0], p, ga);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <int KIND, int QG = -1, int QR = FP4Q_RTNE>
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& dh, const CUtensorMap& df,
+                        const GemmParams& p, cudaStream_t s) {
+  using KK = KindK<KIND, (QG >= 0)>;
+  static unsigned done = 0;   // one bit per device ordinal < 32
+  static int max_pairs[32] = {};
+  auto kern = bs_gemm_kernel<KIND, QG, QR, false>;
+  int pairs = resident_pairs(kern, KK::kSmem, KK::kThreads, done, max_pairs);
+  if (pairs <= 0) return cudaErrorInvalidConfiguration;
+  const int tiles = ((p.M + TM - 1) / TM) * ((p.N + BN - 1) / BN);
+  if (tiles < pairs) pairs = tiles;
+  return launch_pairs(kern, pairs, KK::kSmem, KK::kThreads, s, a, b, dh, df, p, NoGroupArgs{});
 }
 
 // Static schedule of a grouped launch: tiles taken longest first (a tile
 // costs 4 per K-tile of 256 plus 10 for its epilogue, in about a quarter of a
-// stage's time), each given to the CTA with the least work so far (a binary
-// heap of CTA loads); every CTA's tiles are then stored together, in the
+// stage's time), each given to the pair with the least work so far (a binary
+// heap of pair loads); every pair's tiles are then stored together, in the
 // order it received them.  The last schedule is kept per host thread and
-// reused while the shapes and the CTA count repeat.  Returns the CTA count.
+// reused while the shapes and the pair count repeat.  Returns the pair count.
 int group_schedule(GroupArgs& ga, int units) {
   const int total = ga.tile0[ga.np];
   if (units > total) units = total;
@@ -1113,23 +1016,25 @@ int group_schedule(GroupArgs& ga, int units) {
   return units;
 }
 
+// One launch over the GEMMs of ga; p supplies the status word only.
+template <int KIND>
+cudaError_t launch_gemm_group(GroupArgs& ga, const GemmParams& p, cudaStream_t s) {
+  using KK = KindK<KIND, false>;
+  static unsigned done = 0;
+  static int max_pairs[32] = {};
+  auto kern = bs_gemm_kernel<KIND, -1, FP4Q_RTNE, true>;
+  const int pairs = resident_pairs(kern, KK::kSmem, KK::kThreads, done, max_pairs);
+  if (pairs <= 0) return cudaErrorInvalidConfiguration;
+  const int units = group_schedule(ga, pairs);
+  return launch_pairs(kern, units, KK::kSmem, KK::kThreads, s, ga.a[0], ga.b[0], ga.dh[0], ga.df[0], p, ga);
+}
+
 bool al(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Cooperation form of the plain GEMM kernels, -DFP4Q_GEMM_CLUSTER=0/1:
-// single CTA or cta_group::2 pair.  The fused-quantization kernels use the
-// single form (the pair form is not built for them).
-#ifndef FP4Q_GEMM_CLUSTER
-#define FP4Q_GEMM_CLUSTER 0
-#endif
-constexpr int kCluster = FP4Q_GEMM_CLUSTER;
-static_assert(kCluster == CL_SINGLE || kCluster == CL_PAIR, "FP4Q_GEMM_CLUSTER");
-template <int QG>
-constexpr int cluster_form() { return (kCluster == CL_PAIR && QG >= 0) ? CL_SINGLE : kCluster; }
-
-// Checks shared by the two entry points, the kernel parameters and the
-// operand / output tensor maps.  Returns FP4Q_OK or the error status.
+// Checks shared by the entry points, the kernel parameters and the operand /
+// output tensor maps.  Returns FP4Q_OK or the error status.
 int32_t prepare_gemm(const fp4q_operand* A, const fp4q_operand* B, int64_t M, int64_t N, int64_t K, int32_t grid,
-                     int32_t scale, void* D_bf16, float* D_f32, uint32_t* d_status, int cl, bool fused, int& kind,
+                     int32_t scale, void* D_bf16, float* D_f32, uint32_t* d_status, bool fused, int& kind,
                      GemmParams& p, CUtensorMap& ta, CUtensorMap& tb, CUtensorMap& tdh, CUtensorMap& tdf) {
   if (!A || !B) return FP4Q_ERR_INVALID_ARG;
   if (grid != FP4Q_GRID_E2M1 && grid != FP4Q_GRID_E1M2 && grid != FP4Q_GRID_E2M1_R4) return FP4Q_ERR_INVALID_ARG;
@@ -1153,29 +1058,27 @@ int32_t prepare_gemm(const fp4q_operand* A, const fp4q_operand* B, int64_t M, in
   p.ts_a = A->tensor_scale;
   p.ts_b = B->tensor_scale;
   p.status = d_status;
+  p.want_bf16 = D_bf16 != nullptr;
+  p.want_f32 = D_f32 != nullptr;
   p.M = (int32_t)M;
   p.N = (int32_t)N;
   p.K = (int32_t)K;
-  p.want_bf16 = D_bf16 != nullptr;
-  p.want_f32 = D_f32 != nullptr;
   memset(&tdh, 0, sizeof(tdh));
   memset(&tdf, 0, sizeof(tdf));
-  if (!make_map(&ta, a_data, row_bytes, (uint64_t)M, BM) ||
-      !make_map(&tb, b_data, row_bytes, (uint64_t)N, cl == CL_SINGLE ? 256u : 128u))
+  if (!make_map(&ta, a_data, row_bytes, (uint64_t)M) || !make_map(&tb, b_data, row_bytes, (uint64_t)N))
     return FP4Q_ERR_CUDA;
-  if (D_bf16 && !make_out_map(&tdh, D_bf16, (uint64_t)N, (uint64_t)M, false, fused ? 128u : (uint32_t)kPlainBoxBytes))
+  if (D_bf16 && !make_out_map(&tdh, D_bf16, (uint64_t)N, (uint64_t)M, false, fused ? kFusedBox : kPlainBox))
     return FP4Q_ERR_CUDA;
-  if (D_f32 && !make_out_map(&tdf, D_f32, (uint64_t)N, (uint64_t)M, true, (uint32_t)kPlainBoxBytes)) return FP4Q_ERR_CUDA;
+  if (D_f32 && !make_out_map(&tdf, D_f32, (uint64_t)N, (uint64_t)M, true, kPlainBox)) return FP4Q_ERR_CUDA;
   return FP4Q_OK;
 }
 
 template <int QG, int QR>
 cudaError_t launch_kind(int kind, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tdh,
                         const CUtensorMap& tdf, const GemmParams& p, cudaStream_t s) {
-  constexpr int cl = cluster_form<QG>();
-  if (kind == KIND_MXF4) return launch_gemm<KIND_MXF4, cl, QG, QR>(ta, tb, tdh, tdf, p, s);
-  if (kind == KIND_NVF4) return launch_gemm<KIND_NVF4, cl, QG, QR>(ta, tb, tdh, tdf, p, s);
-  return launch_gemm<KIND_F8, cl, QG, QR>(ta, tb, tdh, tdf, p, s);
+  if (kind == KIND_MXF4) return launch_gemm<KIND_MXF4, QG, QR>(ta, tb, tdh, tdf, p, s);
+  if (kind == KIND_NVF4) return launch_gemm<KIND_NVF4, QG, QR>(ta, tb, tdh, tdf, p, s);
+  return launch_gemm<KIND_F8, QG, QR>(ta, tb, tdh, tdf, p, s);
 }
 
 }  // namespace
@@ -1189,8 +1092,8 @@ extern "C" int32_t fp4q_gemm(const fp4q_operand* A, const fp4q_operand* B, int64
   int kind = 0;
   GemmParams p;
   CUtensorMap ta, tb, tdh, tdf;
-  const int32_t st = prepare_gemm(A, B, M, N, K, grid, scale, D_bf16, D_f32, d_status, cluster_form<-1>(), false,
-                                  kind, p, ta, tb, tdh, tdf);
+  const int32_t st =
+      prepare_gemm(A, B, M, N, K, grid, scale, D_bf16, D_f32, d_status, false, kind, p, ta, tb, tdh, tdf);
   if (st != FP4Q_OK) return st;
   const cudaError_t e = launch_kind<-1, FP4Q_RTNE>(kind, ta, tb, tdh, tdf, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
@@ -1210,29 +1113,28 @@ extern "C" int32_t fp4q_gemm_group(const fp4q_gemm_problem* problems, int32_t co
     const fp4q_gemm_problem& q = problems[i];
     if (!q.D_bf16 && !q.D_f32) return FP4Q_ERR_INVALID_ARG;
     GemmParams pi;
-    const int32_t st = prepare_gemm(q.A, q.B, q.M, q.N, q.K, grid, scale, q.D_bf16, q.D_f32, d_status, CL_SINGLE,
-                                    false, kind, pi, ga.a[i], ga.b[i], ga.dh[i], ga.df[i]);
+    const int32_t st = prepare_gemm(q.A, q.B, q.M, q.N, q.K, grid, scale, q.D_bf16, q.D_f32, d_status, false, kind,
+                                    pi, ga.a[i], ga.b[i], ga.dh[i], ga.df[i]);
     if (st != FP4Q_OK) return st;
     if (i == 0) p0 = pi;
     ga.sfa[i] = pi.sfa;
     ga.sfb[i] = pi.sfb;
     ga.ts_a[i] = pi.ts_a;
     ga.ts_b[i] = pi.ts_b;
+    ga.want_bf16[i] = pi.want_bf16;
+    ga.want_f32[i] = pi.want_f32;
     ga.M[i] = pi.M;
     ga.N[i] = pi.N;
     ga.K[i] = pi.K;
-    ga.want_bf16[i] = pi.want_bf16;
-    ga.want_f32[i] = pi.want_f32;
-    const int64_t tiles = (q.M / BM) * ((q.N + BN - 1) / BN);
+    const int64_t tiles = ((q.M + TM - 1) / TM) * ((q.N + BN - 1) / BN);
     if (ga.tile0[i] + tiles > kGroupMaxTiles) return FP4Q_ERR_UNSUPPORTED;
     ga.tile0[i + 1] = ga.tile0[i] + (int32_t)tiles;
   }
-  const int units = group_schedule(ga, num_sms());
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (kind == KIND_MXF4) e = launch_gemm_group<KIND_MXF4>(ga, units, p0, s);
-  else if (kind == KIND_NVF4) e = launch_gemm_group<KIND_NVF4>(ga, units, p0, s);
-  else e = launch_gemm_group<KIND_F8>(ga, units, p0, s);
+  if (kind == KIND_MXF4) e = launch_gemm_group<KIND_MXF4>(ga, p0, s);
+  else if (kind == KIND_NVF4) e = launch_gemm_group<KIND_NVF4>(ga, p0, s);
+  else e = launch_gemm_group<KIND_F8>(ga, p0, s);
   return e == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
 }
 
@@ -1254,8 +1156,8 @@ extern "C" int32_t fp4q_gemm_quantize(const fp4q_operand* A, const fp4q_operand*
   int kind = 0;
   GemmParams p;
   CUtensorMap ta, tb, tdh, tdf;
-  const int32_t st = prepare_gemm(A, B, M, N, K, grid, scale, D_bf16, nullptr, d_status, cluster_form<0>(), true,
-                                  kind, p, ta, tb, tdh, tdf);
+  const int32_t st =
+      prepare_gemm(A, B, M, N, K, grid, scale, D_bf16, nullptr, d_status, true, kind, p, ta, tb, tdh, tdf);
   if (st != FP4Q_OK) return st;
   p.q_codes = out->codes;
   p.q_scales = out->scales;

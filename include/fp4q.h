@@ -197,7 +197,7 @@ int32_t fp4q_gemm(const fp4q_operand* A, const fp4q_operand* B, int64_t M, int64
  *  problems  count descriptions, each as fp4q_gemm's arguments (A, B, M, N, K,
  *           D_bf16, D_f32; at least one output each)
  *  count    1 .. 4
- *  Returns FP4Q_ERR_UNSUPPORTED when the GEMMs have more than 8192 128 x 256
+ *  Returns FP4Q_ERR_UNSUPPORTED when the GEMMs have more than 8192 256 x 256
  *  tiles together (call fp4q_gemm for each then), otherwise as fp4q_gemm.
  *  The outputs must not overlap one another or the inputs. */
 typedef struct {
