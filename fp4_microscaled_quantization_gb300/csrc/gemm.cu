@@ -19,17 +19,18 @@
 //   warp 0      producer: A rows and this CTA's half of B by
 //               cp.async.bulk.tensor (.cta_group::2, 128-byte swizzled
 //               K-major rows) into a ring of kStages slots, the bytes
-//               completing on the leader's full barrier of the slot; and the
-//               stage's scale chunks (below).
+//               completing on the leader's full barrier of the slot (two TMA
+//               instructions per stage: issuing them is not free, so the
+//               scale chunks have a loader of their own).
 //   warp 1      owns the TMEM allocation (cta_group::2); on the leader one
 //               lane waits for a stage (one barrier: both CTAs' operands and
 //               both CTAs' scale writers), issues its MMAs back to back and
 //               frees the stage with one tcgen05.commit (multicast to both
 //               CTAs).  The tensor pipe queues only about one MMA ahead of
 //               the lane, so the lane does nothing else between stages.
-//   warps 6-9   scale writers, one per TMEM lane quarter.  The producer
+//   warps 6-9   scale writers, one per TMEM lane quarter.  The last warp
 //               loads a stage's compact 512-byte scale chunks into the slot
-//               with its operands (cp.async.bulk, completing on a barrier of
+//               beside its operands (cp.async.bulk, completing on a barrier of
 //               this CTA); every writer copies its rows of the chunks into the
 //               stage's TMEM scale slot with tcgen05.st and arrives on the
 //               stage's barrier in the leader.
@@ -111,10 +112,12 @@ struct KindK {
   static constexpr int kSfCols = KIND == KIND_MXF4 ? 32 : (KIND == KIND_NVF4 ? 48 : 16);
   // every stage has its TMEM scale slot beside the accumulator
   static constexpr int kStagesTmem = (int)(TMEM_COLS - 256) / kSfCols;
-  // threads: producer, MMA, scale-writer warps and the epilogue warps (8, two
-  // per TMEM lane quarter; 4 in the kernels that quantize their output)
+  // threads: producer, MMA, scale-writer warps, the epilogue warps (8, two
+  // per TMEM lane quarter; 4 in the kernels that quantize their output) and
+  // the scale-chunk loader (the last warp)
   static constexpr int kEpiWarps = FUSED ? 4 : 8;
-  static constexpr int kThreads = 32 * (6 + kEpiWarps);
+  static constexpr int kThreads = 32 * (7 + kEpiWarps);
+  static constexpr int kChunkWarp = 6 + kEpiWarps;
   static constexpr int kEpiCols = 256 / (kEpiWarps / 4);   // accumulator columns per epilogue warp
   // shared-memory staging of an epilogue warp: one 32-row x 32-byte store box
   // (plain kernels), or the warp's whole 32 x 256 bf16 slice of the tile
@@ -466,7 +469,7 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_full + 8 * s, 10);     // both producers' expect_tx and the 8 scale-writer warps
       mbar_init(bar_empty + 8 * s, 1);     // the leader's commit
-      mbar_init(bar_sfd + 8 * s, 1);       // this CTA's producer
+      mbar_init(bar_sfd + 8 * s, 1);       // this CTA's chunk loader
     }
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_empty, 2 * KK::kEpiWarps);   // one arrival per epilogue warp of both CTAs
@@ -506,19 +509,6 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
         const TileCtx t = tile_ctx(w);
         const CUtensorMap* mA = map_a(t.gi);
         const CUtensorMap* mB = map_b(t.gi);
-        const bool rows = t.m0 < t.M;          // false only for the second CTA of a 128-row tail
-        const bool rg1 = (t.n0 + 128) < t.N;   // the tile's second 128-row group of B exists
-        const uint8_t* sfa_g;
-        const uint8_t* sfb_g;
-        if constexpr (GROUP) {
-          sfa_g = ga.sfa[t.gi];
-          sfb_g = ga.sfb[t.gi];
-        } else {
-          sfa_g = p.sfa;
-          sfb_g = p.sfb;
-        }
-        const uint8_t* sfa_t = sfa_g + (size_t)(t.m0 / 128) * t.nq * 512;
-        const uint8_t* sfb_t = sfb_g + (size_t)(t.n0 / 128) * t.nq * 512;
         for (int kt = 0; kt < t.num_kt; ++kt, ++it) {
           const int s = (int)(it % S);
           if (!mbar_wait(bar_empty + 8 * s, ((it / S) & 1u) ^ 1u, abort_flag)) {
@@ -531,14 +521,6 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
           // rows past M or N (a 128-row tail) are zero-filled and still counted
           tma_load_2d_pair(st, mA, kt * KROW, t.m0, fb);
           tma_load_2d_pair(st + A_BYTES, mB, kt * KROW, t.n0 + 128 * (int)rank, fb);
-          // this CTA's scale chunks of the stage, for its scale writers
-          const int q0 = kt * KK::kChunks;
-          const uint32_t sf_bytes = (uint32_t)min(KK::kChunks, t.nq - q0) * 512u;
-          const uint32_t sb = bar_sfd + 8 * s, ca = st + OP_STAGE;
-          mbar_expect_tx(sb, sf_bytes * ((rows ? 1u : 0u) + (rg1 ? 2u : 1u)));
-          if (rows) bulk_load(ca, sfa_t + (size_t)q0 * 512, sf_bytes, sb);
-          bulk_load(ca + KK::kChunks * 512, sfb_t + (size_t)q0 * 512, sf_bytes, sb);
-          if (rg1) bulk_load(ca + 2 * KK::kChunks * 512, sfb_t + ((size_t)t.nq + q0) * 512, sf_bytes, sb);
         }
       }
       // The leader's commits arrive on this CTA's empty barriers: wait for the
@@ -614,6 +596,48 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
                    : "memory");
       const uint64_t t0 = globaltimer();
       while (!mbar_try(bar_drain, 0) && globaltimer() - t0 < 2000000000ull) {
+      }
+    }
+    __syncwarp();
+  } else if (warp == KK::kChunkWarp) {
+    if (lane == 0) {
+      // ---------------- scale-chunk loader: a stage's compact chunks of this
+      // CTA into its slot, once the slot's previous MMAs finished
+      uint32_t it = 0;
+      bool ok = true;
+      for (int w = w_begin; w < w_end && ok; w += w_step) {
+        const TileCtx t = tile_ctx(w);
+        const bool rows = t.m0 < t.M;          // false only for the second CTA of a 128-row tail
+        const bool rg1 = (t.n0 + 128) < t.N;   // the tile's second 128-row group of B exists
+        const uint8_t* sfa_g;
+        const uint8_t* sfb_g;
+        if constexpr (GROUP) {
+          sfa_g = ga.sfa[t.gi];
+          sfb_g = ga.sfb[t.gi];
+        } else {
+          sfa_g = p.sfa;
+          sfb_g = p.sfb;
+        }
+        const uint8_t* sfa_t = sfa_g + (size_t)(t.m0 / 128) * t.nq * 512;
+        const uint8_t* sfb_t = sfb_g + (size_t)(t.n0 / 128) * t.nq * 512;
+        for (int kt = 0; kt < t.num_kt; ++kt, ++it) {
+          const int s = (int)(it % S);
+          if (!mbar_wait(bar_empty + 8 * s, ((it / S) & 1u) ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int q0 = kt * KK::kChunks;
+          const uint32_t sf_bytes = (uint32_t)min(KK::kChunks, t.nq - q0) * 512u;
+          const uint32_t sb = bar_sfd + 8 * s, ca = sbase + (uint32_t)s * SLOT + OP_STAGE;
+          mbar_expect_tx(sb, sf_bytes * ((rows ? 1u : 0u) + (rg1 ? 2u : 1u)));
+          if (rows) bulk_load(ca, sfa_t + (size_t)q0 * 512, sf_bytes, sb);
+          bulk_load(ca + KK::kChunks * 512, sfb_t + (size_t)q0 * 512, sf_bytes, sb);
+          if (rg1) bulk_load(ca + 2 * KK::kChunks * 512, sfb_t + ((size_t)t.nq + q0) * 512, sf_bytes, sb);
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        raise_status(p.status, FP4Q_DEV_TIMEOUT);
       }
     }
     __syncwarp();
