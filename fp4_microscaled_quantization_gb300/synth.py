@@ -134,3 +134,23 @@ def layer(tokens: int = 16384, d_in: int = 4096, d_out: int = 4096, seed: int = 
     W = weight_w(d_out, d_in, seed * 10 + 2)
     dY = grad_dy(tokens, d_out, seed * 10 + 3)
     return X, W, dY
+
+
+def grid_valued(rows: int, cols: int, seed: int, grid: int = 0) -> np.ndarray:
+    """Entries drawn uniformly from the signed levels of a 4-bit grid (0: E2M1
+    {0, .5, 1, 1.5, 2, 3, 4, 6}; 1: E1M2 {k/4}), with one seeded position of
+    every 32-element row block set to a level of the grid's top binade (E2M1
+    4 or 6; E1M2 1 .. 1.75).  Every block's power-of-two scale is then 1 and
+    the values are their own quantization, so products of two such matrices
+    are multiples of 1/4 (E2M1) or 1/16 (E1M2) whose sums stay exact in fp32
+    for K <= 4096."""
+    g = _rng(seed)
+    levels = (np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], np.float32) if grid == 0
+              else np.arange(8, dtype=np.float32) / np.float32(4.0))
+    top = levels[6:] if grid == 0 else levels[4:]
+    x = levels[g.integers(0, 8, (rows, cols))]
+    nb = cols // 32
+    pos = g.integers(0, 32, (rows, nb)) + 32 * np.arange(nb)[None, :]
+    x[np.arange(rows)[:, None], pos] = top[g.integers(0, top.size, (rows, nb))]
+    x *= np.where(g.random((rows, cols)) < 0.5, -1.0, 1.0).astype(np.float32)
+    return to_bf16_bits(x)

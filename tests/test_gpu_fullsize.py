@@ -8,7 +8,8 @@ times (32 x 256 quantizer tiles, 128 x 256 GEMM tiles):
   weight  W 14336x4096, both copies, H32, NVFP4-style E2M1 and E1M2, RTNE,
           two-pass (amax pre-pass) and one-pass (caller's amax)
   layer   X 16384x4096, W 4096^2, dY 16384x4096: all six copies bit-exact, and
-          the Fprop / Dgrad / Wgrad GEMMs on 4096 sampled outputs per GEMM
+          the Fprop / Dgrad / Wgrad GEMMs (Dgrad and Wgrad in one grouped launch)
+          on 4096 sampled outputs per GEMM, for each of the three MMA kinds
 
 Every quantized copy is compared in full, bit for bit.  The oracle runs in
 threads (its C calls release the GIL)."""
@@ -128,12 +129,25 @@ def test_weight_nv_two_and_one_pass(fq, orc, grid):
     assert_same(cfg1, c1, refs[1])
 
 
-def test_layer_operands_and_gemms(fq, orc):
+@pytest.mark.parametrize("kind", ["mxf4", "nvf4", "mxf8f6f4"])
+def test_layer_operands_and_gemms(fq, orc, kind):
+    """All six copies of the layer's operands bit-exact, then Fprop (fp4q_gemm)
+    and Dgrad + Wgrad in one grouped launch (fp4q_gemm_group, as the benchmark
+    runs them) on 4096 sampled outputs each against the oracle's fp64 GEMM of
+    the oracle's own copies, for each MMA kind: E2M1 with MX scales
+    (kind::mxf4), E2M1 with NVFP4-style scales (kind::mxf4nvf4, alpha =
+    S_t(A) S_t(B)) and E1M2 through its E4M3 bytes (kind::mxf8f6f4)."""
     X, W, dY = synth.layer()
+    grid = 1 if kind == "mxf8f6f4" else 0
+    scale = fq.SCALE_NV if kind == "nvf4" else fq.SCALE_MX
+    e4 = grid == 1
     mK, mN, mM = (orc.sign_mask_from_seed(1005 + i, 16) for i in range(3))
-    cfg_x = fq.Config(rot=16, sign_mask_row=mK, sign_mask_col=mM, sf_layout=fq.SF_MMA)
-    cfg_w = fq.Config(rot=16, sign_mask_row=mK, sign_mask_col=mN, sf_layout=fq.SF_MMA)
-    cfg_g = fq.Config(rot=16, sign_mask_row=mN, sign_mask_col=mM, round=fq.SR, sr_seed=1008, sf_layout=fq.SF_MMA)
+    cfg_x = fq.Config(grid=grid, scale=scale, rot=16, sign_mask_row=mK, sign_mask_col=mM, sf_layout=fq.SF_MMA,
+                      emit_e4m3=e4)
+    cfg_w = fq.Config(grid=grid, scale=scale, rot=16, sign_mask_row=mK, sign_mask_col=mN, sf_layout=fq.SF_MMA,
+                      emit_e4m3=e4)
+    cfg_g = fq.Config(grid=grid, scale=scale, rot=16, sign_mask_row=mN, sign_mask_col=mM, round=fq.SR, sr_seed=1008,
+                      sf_layout=fq.SF_MMA, emit_e4m3=e4)
     ox, fx = quantize_both(fq, orc, X, cfg_x)
     ow, fw = quantize_both(fq, orc, W, cfg_w)
     og, fg = quantize_both(fq, orc, dY, cfg_g)
@@ -142,18 +156,24 @@ def test_layer_operands_and_gemms(fq, orc):
         for o in (0, 1):
             refs[(name, o)] = futs[o].result()
             assert_same(cfg, ops[o], refs[(name, o)])
-    deq = {k: orc.dequantize(v["codes"], v["scales"], 0, 0, 0) for k, v in refs.items()}
+    deq = {k: orc.dequantize(v["codes"], v["scales"], v["tensor_scale"], grid, scale, with_tensor_scale=False)
+           for k, v in refs.items()}
+    ts = {k: v["tensor_scale"] for k, v in refs.items()}
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _, Yf = fq.gemm(ox[0], ow[0], grid, scale, want_bf16=False, status=st)
+    (_, dXf), (_, dWf) = fq.gemm_group([(og[0], ow[1]), (og[1], ox[1])], grid, scale, want_bf16=False,
+                                       want_f32=True, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
     rng = np.random.default_rng(0)
-    cases = {"fprop": (ox[0], ow[0], ("x", 0), ("w", 0)),
-             "dgrad": (og[0], ow[1], ("g", 0), ("w", 1)),
-             "wgrad": (og[1], ox[1], ("g", 1), ("x", 1))}
-    for name, (A, B, ka, kb) in cases.items():
-        Dh, Df = fq.gemm(A, B, 0, 0)
-        torch.cuda.synchronize()
-        ii = rng.integers(0, A.rows, 4096)
-        jj = rng.integers(0, B.rows, 4096)
-        want = orc.gemm_entries(deq[ka], deq[kb], ii, jj)
+    cases = {"fprop": (Yf, ("x", 0), ("w", 0)), "dgrad": (dXf, ("g", 0), ("w", 1)),
+             "wgrad": (dWf, ("g", 1), ("x", 1))}
+    for name, (Df, ka, kb) in cases.items():
+        ii = rng.integers(0, Df.shape[0], 4096)
+        jj = rng.integers(0, Df.shape[1], 4096)
+        alpha = float(np.float64(ts[ka]) * np.float64(ts[kb])) if scale == fq.SCALE_NV else 1.0
+        want = orc.gemm_entries(deq[ka], deq[kb], ii, jj, alpha)
         got = Df[torch.from_numpy(ii).cuda(), torch.from_numpy(jj).cuda()].double().cpu().numpy()
         rel = np.linalg.norm(got - want) / np.linalg.norm(want)
-        assert rel <= 1e-3, f"{name}: sampled relative Frobenius error {rel:.3e}"
-        print(f"{name}: sampled rel err {rel:.2e}")
+        assert rel <= 1e-3, f"{kind} {name}: sampled relative Frobenius error {rel:.3e}"
+        print(f"{kind} {name}: sampled rel err {rel:.2e}")

@@ -100,6 +100,17 @@ def test_philox_known_answers(orc):
         assert [int(v) for v in orc.philox4x32_10(ctr, key)] == want
 
 
+def test_sign_mask_is_word0_of_philox_at_its_counter(orc):
+    """The sign mask of a seed is word 0 of Philox4x32-10 with key (lo32, hi32)
+    of the seed at counter (0, 0, 0x5349474E, 0), masked to n_h bits: the
+    reading the oracle states, checked against the known-answer-pinned Philox
+    (a different word, counter or key half would fail here)."""
+    for seed in (0, 1, 7, 1005, 0xDEADBEEF, 2 ** 40 + 3, 2 ** 64 - 1):
+        w = orc.philox4x32_10([0, 0, 0x5349474E, 0], [seed & 0xFFFFFFFF, seed >> 32])
+        for n in (16, 32):
+            assert orc.sign_mask_from_seed(seed, n) == int(w[0]) & ((1 << n) - 1), (seed, n)
+
+
 def test_sign_mask_bits_and_determinism(orc):
     for n in (16, 32):
         masks = [orc.sign_mask_from_seed(s, n) for s in range(64)]
