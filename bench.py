@@ -133,8 +133,64 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ our arm
+# The two recipes of one linear layer's step ("Repensando o Vies de
+# Encolhimento", Metodologia 2): E2M1 GEMMs on kind::mxf4; UFP4 = the uniform
+# E1M2 grid, whose GEMMs run kind::mxf8f6f4 on the exact E4M3 bytes of the
+# codes (one more byte per element and copy written by the quantizer).
+RECIPES = {"e2m1": {"grid": 0, "e4m3": False, "mma": "kind::mxf4 (FP4)", "flop_ratio": 13.5 / 2.25,
+                    "mma_flop_clk_sm": 32768},
+           "ufp4": {"grid": 1, "e4m3": True, "mma": "kind::mxf8f6f4 (FP8 E4M3 bytes of E1M2 codes)",
+                    "flop_ratio": 4.5 / 2.25, "mma_flop_clk_sm": 16384}}
+
+
+def recipe_buffers(fp4q, recipe, dev):
+    """Configs (random H16 with signs shared along each contraction axis, RTNE on
+    X and W, Philox SR on dY, MMA scale layout) and the six copies and three
+    outputs of one recipe."""
+    grid, e4 = RECIPES[recipe]["grid"], RECIPES[recipe]["e4m3"]
+    mK = fp4q.sign_mask_from_seed(SEED, 16)
+    mN = fp4q.sign_mask_from_seed(SEED + 1, 16)
+    mM = fp4q.sign_mask_from_seed(SEED + 2, 16)
+    cx = fp4q.Config(grid=grid, rot=16, sign_mask_row=mK, sign_mask_col=mM, sf_layout=fp4q.SF_MMA, emit_e4m3=e4)
+    cw = fp4q.Config(grid=grid, rot=16, sign_mask_row=mK, sign_mask_col=mN, sf_layout=fp4q.SF_MMA, emit_e4m3=e4)
+    cg = fp4q.Config(grid=grid, rot=16, sign_mask_row=mN, sign_mask_col=mM, round=fp4q.SR, sr_seed=SEED + 3,
+                     sf_layout=fp4q.SF_MMA, emit_e4m3=e4)
+    import torch
+    b = {"grid": grid, "cfg": (cx, cw, cg),
+         "Xr": fp4q.alloc_operand(TOKENS, D_IN, cx, dev), "Xc": fp4q.alloc_operand(D_IN, TOKENS, cx, dev),
+         "Wr": fp4q.alloc_operand(D_OUT, D_IN, cw, dev), "Wc": fp4q.alloc_operand(D_IN, D_OUT, cw, dev),
+         "Gr": fp4q.alloc_operand(TOKENS, D_OUT, cg, dev), "Gc": fp4q.alloc_operand(D_OUT, TOKENS, cg, dev),
+         "Y": torch.empty((TOKENS, D_OUT), dtype=torch.bfloat16, device=dev),
+         "dX": torch.empty((TOKENS, D_IN), dtype=torch.bfloat16, device=dev),
+         "dW": torch.empty((D_OUT, D_IN), dtype=torch.bfloat16, device=dev)}
+    b["bytes_per_elem"] = MX_BYTES_PER_ELEM + (2.0 if e4 else 0.0)
+    return b
+
+
+def pct(v):
+    v = sorted(v)
+    return {"p10_us": round(v[len(v) // 10] * 1e6, 2), "median_us": round(v[len(v) // 2] * 1e6, 2),
+            "p90_us": round(v[(9 * len(v)) // 10] * 1e6, 2)}
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def run_ours(args, world, rank, local):
-    import numpy as np
     import torch
 
     from fp4_microscaled_quantization_gb300 import fp4q, synth
@@ -146,196 +202,160 @@ def run_ours(args, world, rank, local):
         os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
     bf16_peak = peaks.get("bf16_tflops", 1900.0)
-    fp4_peak = bf16_peak * (13.5 / 2.25)     # nominal dense FP4 : BF16 ratio on GB300
     peak_src = "measured" if peaks else "fallback"
+    props = torch.cuda.get_device_properties(dev)
+    n_sm = props.multi_processor_count
+    sm_max_mhz = peaks.get("sm_max_mhz", 2070.0)
 
     # ---------------- inputs (bf16, resident)
     Xb, Wb, dYb = synth.layer(TOKENS, D_IN, D_OUT, SEED)
     X, W, dY = (synth.as_torch(a).to(dev) for a in (Xb, Wb, dYb))
-    mK = fp4q.sign_mask_from_seed(SEED, 16)
-    mN = fp4q.sign_mask_from_seed(SEED + 1, 16)
-    mM = fp4q.sign_mask_from_seed(SEED + 2, 16)
-    cfg_x = fp4q.Config(grid=fp4q.GRID_E2M1, rot=16, sign_mask_row=mK, sign_mask_col=mM, sf_layout=fp4q.SF_MMA)
-    cfg_w = fp4q.Config(grid=fp4q.GRID_E2M1, rot=16, sign_mask_row=mK, sign_mask_col=mN, sf_layout=fp4q.SF_MMA)
-    cfg_g = fp4q.Config(grid=fp4q.GRID_E2M1, rot=16, sign_mask_row=mN, sign_mask_col=mM, round=fp4q.SR,
-                        sr_seed=SEED + 3, sf_layout=fp4q.SF_MMA)
-    Xr, Xc = fp4q.alloc_operand(TOKENS, D_IN, cfg_x, dev), fp4q.alloc_operand(D_IN, TOKENS, cfg_x, dev)
-    Wr, Wc = fp4q.alloc_operand(D_OUT, D_IN, cfg_w, dev), fp4q.alloc_operand(D_IN, D_OUT, cfg_w, dev)
-    Gr, Gc = fp4q.alloc_operand(TOKENS, D_OUT, cfg_g, dev), fp4q.alloc_operand(D_OUT, TOKENS, cfg_g, dev)
-    Y = torch.empty((TOKENS, D_OUT), dtype=torch.bfloat16, device=dev)
-    dX = torch.empty((TOKENS, D_IN), dtype=torch.bfloat16, device=dev)
-    dW = torch.empty((D_OUT, D_IN), dtype=torch.bfloat16, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > 129 MB L2
-
-    q_bytes = MX_BYTES_PER_ELEM * (TOKENS * D_IN + D_OUT * D_IN + TOKENS * D_OUT)
+    elems = TOKENS * D_IN + D_OUT * D_IN + TOKENS * D_OUT
     flops = 3 * 2.0 * TOKENS * D_IN * D_OUT
     launches_per_step = 5      # 3 quantizer launches, Fprop, the grouped Dgrad + Wgrad
+    rb = {r: recipe_buffers(fp4q, r, dev) for r in RECIPES}
 
     ev = lambda: torch.cuda.Event(enable_timing=True)
-    kq = {"x": [], "w": [], "g": []}
-    kg = {"fprop": [], "dgrad_wgrad": []}
 
-    def quantize_phase(rec=None):
-        e = [ev() for _ in range(4)] if rec is not None else None
+    def quantize_phase(b, e=None):
+        cx, cw, cg = b["cfg"]
         if e: e[0].record(stream)
-        fp4q.rht_quantize(X, cfg_x, Xr, Xc, status=status, stream=stream)
+        fp4q.rht_quantize(X, cx, b["Xr"], b["Xc"], status=status, stream=stream)
         if e: e[1].record(stream)
-        fp4q.rht_quantize(W, cfg_w, Wr, Wc, status=status, stream=stream)
+        fp4q.rht_quantize(W, cw, b["Wr"], b["Wc"], status=status, stream=stream)
         if e: e[2].record(stream)
-        fp4q.rht_quantize(dY, cfg_g, Gr, Gc, status=status, stream=stream)
+        fp4q.rht_quantize(dY, cg, b["Gr"], b["Gc"], status=status, stream=stream)
         if e: e[3].record(stream)
-        if rec is not None:
-            rec.append(("q", e))
 
-    def gemm_phase(rec=None):
+    def gemm_phase(b, e=None):
         # Fprop, then the backward GEMMs (Dgrad, Wgrad) in one grouped launch
-        e = [ev() for _ in range(3)] if rec is not None else None
         if e: e[0].record(stream)
-        fp4q.gemm(Xr, Wr, fp4q.GRID_E2M1, fp4q.SCALE_MX, want_f32=False, D_bf16=Y, status=status, stream=stream)
+        fp4q.gemm(b["Xr"], b["Wr"], b["grid"], fp4q.SCALE_MX, want_f32=False, D_bf16=b["Y"], status=status,
+                  stream=stream)
         if e: e[1].record(stream)
-        fp4q.gemm_group([(Gr, Wc), (Gc, Xc)], fp4q.GRID_E2M1, fp4q.SCALE_MX, want_bf16=True, want_f32=False,
-                        outs=[(dX, None), (dW, None)], status=status, stream=stream)
+        fp4q.gemm_group([(b["Gr"], b["Wc"]), (b["Gc"], b["Xc"])], b["grid"], fp4q.SCALE_MX, want_bf16=True,
+                        want_f32=False, outs=[(b["dX"], None), (b["dW"], None)], status=status, stream=stream)
         if e: e[2].record(stream)
-        if rec is not None:
-            rec.append(("g", e))
+
+    def timed_steps(b, steps):
+        recs = []
+        for _ in range(steps):
+            flush.zero_()        # outside the events: evict the previous step from L2
+            eq, eg = [ev() for _ in range(4)], [ev() for _ in range(3)]
+            quantize_phase(b, eq)
+            gemm_phase(b, eg)
+            recs.append((eq, eg))
+        return recs
+
+    def summarize(recs):
+        kq = {"x": [], "w": [], "g": []}
+        kg = {"fprop": [], "dgrad_wgrad": []}
+        q_times, g_times = [], []
+        for eq, eg in recs:
+            pq = [eq[i].elapsed_time(eq[i + 1]) * 1e-3 for i in range(3)]
+            pg = [eg[i].elapsed_time(eg[i + 1]) * 1e-3 for i in range(2)]
+            q_times.append(sum(pq))
+            g_times.append(sum(pg))
+            for k, t in zip(kq, pq):
+                kq[k].append(t)
+            for k, t in zip(kg, pg):
+                kg[k].append(t)
+        return q_times, g_times, kq, kg
 
     for _ in range(args.warmup):
-        flush.zero_()
-        quantize_phase()
-        gemm_phase()
+        for r in RECIPES:
+            flush.zero_()
+            quantize_phase(rb[r])
+            gemm_phase(rb[r])
     torch.cuda.synchronize(dev)
     if status.item() != 0:
         raise RuntimeError(f"device status {status.item():#x} during warm-up")
 
     bus = None
     try:
-        props = torch.cuda.get_device_properties(dev)
         bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
     except AttributeError:
         pass
     clocks = ClockSampler(bus)
     clocks.start()
     time.sleep(0.3)
-    recs = []
     barrier(world, dev)
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
-    for _ in range(args.steps):
-        flush.zero_()        # outside the events: evict the previous step from L2
-        quantize_phase(recs)
-        gemm_phase(recs)
+    recs = timed_steps(rb["e2m1"], args.steps)          # the timed region of the headline metric
     torch.cuda.synchronize(dev)
     barrier(world, dev)
     wall = time.perf_counter() - wall0
+    recs_u = timed_steps(rb["ufp4"], args.steps)        # the second recipe, same step, same sizes
+    torch.cuda.synchronize(dev)
     clk = clocks.stop()
     if status.item() != 0:
         raise RuntimeError(f"device status {status.item():#x} in the timed region")
 
-    q_times, g_times = [], []
-    for kind, e in recs:
-        per = [e[i].elapsed_time(e[i + 1]) * 1e-3 for i in range(len(e) - 1)]
-        (q_times if kind == "q" else g_times).append(sum(per))
-        for key, t in zip(("x", "w", "g") if kind == "q" else ("fprop", "dgrad_wgrad"), per):
-            (kq if kind == "q" else kg)[key].append(t)
+    q_times, g_times, kq, kg = summarize(recs)
     q_s = sum(q_times) / len(q_times)
     g_s = sum(g_times) / len(g_times)
-
-    def pct(v):
-        v = sorted(v)
-        return {"p10_us": round(v[len(v) // 10] * 1e6, 2), "median_us": round(v[len(v) // 2] * 1e6, 2),
-                "p90_us": round(v[(9 * len(v)) // 10] * 1e6, 2)}
+    q_bytes = MX_BYTES_PER_ELEM * elems
     value = aggregate(q_bytes, q_s, world, dev) / 1e9
     gemm_tflops = aggregate(flops, g_s, world, dev) / 1e12
+    clock_mhz = clk.get("sm_mhz") or sm_max_mhz
 
-    # ---------------- end to end through the C ABI from pinned host buffers
-    hX, hW, hdY = (t.cpu().pin_memory() for t in (X, W, dY))
-    hY, hdX, hdW = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (Y, dX, dW))
-    h2d = sum(t.numel() * t.element_size() for t in (hX, hW, hdY))
-    d2h = sum(t.numel() * t.element_size() for t in (hY, hdX, hdW))
-    # host<->device copies run on a copy stream (one copy engine's worth of link
-    # bandwidth: splitting a copy over more streams measured no faster).  The
-    # uploads go in the order dY, X, W so that the longest quantization (dY,
-    # stochastic rounding) overlaps the uploads after it and only W's short one
-    # is left at the end; the download of each GEMM's output overlaps the GEMMs
-    # after it; every compute step waits for its own input's upload
-    copy_stream = torch.cuda.Stream(dev)
-    e2e_q, e2e_g = [], []
-    for it in range(args.warmup + args.steps):
-        flush.zero_()
-        e0, e1, e2 = ev(), ev(), ev()
-        e0.record(stream)
-        copy_stream.wait_event(e0)
-        up = [ev() for _ in range(3)]
-        with torch.cuda.stream(copy_stream):
-            for dst, src, u in ((dY, hdY, up[0]), (X, hX, up[1]), (W, hW, up[2])):
-                dst.copy_(src, non_blocking=True)
-                u.record(copy_stream)
-        for u, (x, cfg, ro, co) in zip(up, ((dY, cfg_g, Gr, Gc), (X, cfg_x, Xr, Xc), (W, cfg_w, Wr, Wc))):
-            stream.wait_event(u)
-            fp4q.rht_quantize(x, cfg, ro, co, status=status, stream=stream)
-        e1.record(stream)
-        fp4q.gemm(Xr, Wr, fp4q.GRID_E2M1, fp4q.SCALE_MX, want_f32=False, D_bf16=Y, status=status, stream=stream)
-        g = ev()
-        g.record(stream)
-        copy_stream.wait_event(g)
-        with torch.cuda.stream(copy_stream):
-            hY.copy_(Y, non_blocking=True)
-        fp4q.gemm_group([(Gr, Wc), (Gc, Xc)], fp4q.GRID_E2M1, fp4q.SCALE_MX, want_bf16=True, want_f32=False,
-                        outs=[(dX, None), (dW, None)], status=status, stream=stream)
-        g = ev()
-        g.record(stream)
-        copy_stream.wait_event(g)
-        with torch.cuda.stream(copy_stream):
-            hdX.copy_(dX, non_blocking=True)
-            hdW.copy_(dW, non_blocking=True)
-        down = ev()
-        down.record(copy_stream)
-        stream.wait_event(down)
-        e2.record(stream)
-        e2.synchronize()
-        if it >= args.warmup:
-            e2e_q.append(e0.elapsed_time(e1) * 1e-3)
-            e2e_g.append(e1.elapsed_time(e2) * 1e-3)
-    e2e_value = aggregate(q_bytes, sum(e2e_q) / len(e2e_q), world, dev) / 1e9
-    e2e_gemm = aggregate(flops, sum(e2e_g) / len(e2e_g), world, dev) / 1e12
-    # the link alone: the same uploads and downloads with no compute (median of 5)
-    link = {}
-    for name, pairs in (("h2d", ((dY, hdY), (X, hX), (W, hW))), ("d2h", ((hY, Y), (hdX, dX), (hdW, dW)))):
-        ts = []
-        for _ in range(5):
-            a, b = ev(), ev()
-            a.record(copy_stream)
-            with torch.cuda.stream(copy_stream):
-                for dst, src in pairs:
-                    dst.copy_(src, non_blocking=True)
-            b.record(copy_stream)
-            b.synchronize()
-            ts.append(a.elapsed_time(b) * 1e-3)
-        link[name] = (h2d if name == "h2d" else d2h) / sorted(ts)[2] / 1e9
-
-    # ---------------- rooflines of the two kernels (per-launch averages).  The
-    # GEMM kernel runs twice a step (Fprop; Dgrad + Wgrad grouped): achieved =
-    # the step's GEMM flops / the two launches' summed durations, traffic = the
-    # mean of the two launches' measured DRAM bytes
-    g_achieved = flops / (statistics.mean(kg["fprop"]) + statistics.mean(kg["dgrad_wgrad"])) / 1e12
-    x_launch = statistics.mean(kq["x"])
-    x_bytes = MX_BYTES_PER_ELEM * TOKENS * D_IN
-    x_achieved = x_bytes / x_launch / 1e9
+    # ---------------- rooflines.  The GEMM kernel runs twice a step (Fprop; the
+    # grouped Dgrad + Wgrad): achieved = the step's GEMM flops / the two
+    # launches' summed mean durations.  Denominators: the measured bf16 GEMM
+    # rate x the nominal dense ratio of the kind (the recipe's rule), and, for
+    # reference, ncu's FP4 peak (49152 flop/clk/SM) and the rate of the MMA
+    # instruction this kernel issues (128 cycles per 128 x 256 x 64 FP4 MMA per
+    # SM, measured), both at the maximum SM clock.
     traffic = read_traffic()
+
+    def gemm_roof(r, kgx, peak_bf16):
+        achieved = flops / (statistics.mean(kgx["fprop"]) + statistics.mean(kgx["dgrad_wgrad"])) / 1e12
+        peak = peak_bf16 * RECIPES[r]["flop_ratio"]
+        mma_peak = RECIPES[r]["mma_flop_clk_sm"] * n_sm * sm_max_mhz * 1e6 / 1e12
+        out = {"kernel": f"bs_gemm_kernel ({RECIPES[r]['mma']}, cta_group::2): Fprop launch + grouped "
+                         "Dgrad/Wgrad launch",
+               "bound": "tensor", "achieved": round(achieved, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+               "frac": round(achieved / peak, 4),
+               "peak_source": f"{peak_src} bf16 burst x {RECIPES[r]['flop_ratio']:.0f} (nominal dense ratio)",
+               "mma_instruction_peak": round(mma_peak, 1), "frac_of_mma_instruction_peak": round(achieved / mma_peak, 4)}
+        if r == "e2m1":
+            ncu_peak = 49152 * n_sm * sm_max_mhz * 1e6 / 1e12
+            out["ncu_fp4_peak"] = round(ncu_peak, 1)
+            out["frac_of_ncu_fp4_peak"] = round(achieved / ncu_peak, 4)
+            g_traffic = traffic.get("gemm_mxf4_fprop_bytes"), traffic.get("gemm_mxf4_group_dgrad_wgrad_bytes")
+            out["traffic"] = (g_traffic[0] + g_traffic[1]) // 2 if all(g_traffic) else None
+        else:
+            out["traffic"] = None
+        out["traffic_source"] = "ncu capture summarised in profiles/dram_traffic.txt (per launch, mean of the two)"
+        return out
+
+    roof_gemm = gemm_roof("e2m1", kg, bf16_peak)
+    q_achieved = q_bytes / q_s / 1e9
+    roof_q = {"kernel": "rht_quant_kernel: the step's three launches (X, W RTNE; dY SR), both copies each",
+              "bound": "hbm", "achieved": round(q_achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+              "frac": round(q_achieved / hbm_peak, 4), "traffic": traffic.get("quant_step_bytes"),
+              "peak_source": f"{peak_src} HBM copy",
+              "per_launch_frac": {k: round(MX_BYTES_PER_ELEM * n / statistics.mean(kq[k]) / 1e9 / hbm_peak, 4)
+                                  for k, n in (("x", TOKENS * D_IN), ("w", D_OUT * D_IN), ("g", TOKENS * D_OUT))}}
     dominant_gemm = sum(g_times) >= sum(q_times)
-    g_traffic = None
-    if "gemm_mxf4_fprop_bytes" in traffic and "gemm_mxf4_group_dgrad_wgrad_bytes" in traffic:
-        g_traffic = (traffic["gemm_mxf4_fprop_bytes"] + traffic["gemm_mxf4_group_dgrad_wgrad_bytes"]) // 2
-    roof_gemm = {"kernel": "bs_gemm_kernel<mxf4> (tcgen05): Fprop launch + grouped Dgrad/Wgrad launch",
-                 "bound": "tensor", "achieved": round(g_achieved, 1),
-                 "peak": round(fp4_peak, 1), "unit": "TFLOP/s", "frac": round(g_achieved / fp4_peak, 4),
-                 "traffic": g_traffic,
-                 "peak_source": f"{peak_src} bf16 burst x 6 (nominal FP4:BF16 dense ratio)"}
-    roof_q = {"kernel": "rht_quant_kernel (X, both copies)", "bound": "hbm", "achieved": round(x_achieved, 1),
-              "peak": hbm_peak, "unit": "GB/s", "frac": round(x_achieved / hbm_peak, 4),
-              "traffic": traffic.get("quant_x_bytes"), "peak_source": f"{peak_src} HBM copy"}
+
+    # ---------------- the UFP4 recipe's step
+    uq, ug, ukq, ukg = summarize(recs_u)
+    u_bytes = rb["ufp4"]["bytes_per_elem"] * elems
+    ufp4 = {"recipe": "UFP4: E1M2 grid, MX b32, random H16 on all three GEMMs, RTNE X/W, SR dY; "
+                      "GEMMs on kind::mxf8f6f4 over the E4M3 bytes of the E1M2 codes",
+            "quantize": {"gb_s": round(u_bytes / statistics.mean(uq) / 1e9, 1), "spread": pct(uq),
+                         "bytes_per_step": u_bytes, "bytes_per_elem": rb["ufp4"]["bytes_per_elem"],
+                         "frac_of_hbm": round(u_bytes / statistics.mean(uq) / 1e9 / hbm_peak, 4),
+                         "per_tensor_us": {k: round(statistics.mean(v) * 1e6, 2) for k, v in ukq.items()}},
+            "gemm": {"tflops": round(flops / statistics.mean(ug) / 1e12, 1), "spread": pct(ug),
+                     "per_gemm_us": {k: round(statistics.mean(v) * 1e6, 2) for k, v in ukg.items()}},
+            "roofline": gemm_roof("ufp4", ukg, bf16_peak),
+            "ms_per_step": round((statistics.mean(uq) + statistics.mean(ug)) * 1e3, 4)}
 
     line = {
         "metric": "fused RHT+FP4 quantize GB/s and % of HBM peak; block-scaled FP4 GEMM TFLOPS",
@@ -355,24 +375,135 @@ def run_ours(args, world, rank, local):
                  "per_gemm_us": {k: round(statistics.mean(v) * 1e6, 2) for k, v in kg.items()}},
         "roofline": roof_gemm if dominant_gemm else roof_q,
         "roofline_other": roof_q if dominant_gemm else roof_gemm,
-        "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "gemm_tflops": round(e2e_gemm, 1),
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "link_h2d_gb_s": round(link["h2d"], 1), "link_d2h_gb_s": round(link["d2h"], 1),
-                "note": "H2D of dY/X/W (in that order) inside the quantize phase, D2H of Y/dX/dW inside the GEMM "
-                        "phase; copies on a second stream overlap the compute that does not depend on them; "
-                        "link_*: the same copies alone"},
+        "ufp4": ufp4,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "wall_s_timed": round(wall, 4),
     }
+    line["e2e"] = end_to_end(args, fp4q, rb["e2m1"], X, W, dY, status, stream, flush, q_bytes, flops, world, dev)
     if not args.no_configs:
-        del hX, hW, hdY, hY, hdX, hdW
+        line["tiny_config"] = tiny_config(dev, stream)
         line["quantizer_configs"] = quant_configs(dev, stream, flush)
-        line["epilogue_fusion"] = epilogue_fusion(dev, stream, flush, X, W, cfg_x, cfg_w)
+        b = rb["e2m1"]
+        line["epilogue_fusion"] = epilogue_fusion(dev, stream, flush, X, W, b["cfg"][0], b["cfg"][1])
         line["recipe_quality"] = recipe_quality(X, W, dY)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
     return line
+
+
+def end_to_end(args, fp4q, b, X, W, dY, status, stream, flush, q_bytes, flops, world, dev):
+    """The E2M1 step through the C ABI from pinned host buffers: the H2D copies
+    of dY, X, W inside the quantize phase, the D2H copies of Y, dX, dW inside
+    the GEMM phase, on a copy stream that overlaps the compute not waiting for
+    them.  Median (and p10/p90) over the timed steps, after at least ten
+    untimed ones (the first uploads into freshly pinned buffers are slow)."""
+    import torch
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    cx, cw, cg = b["cfg"]
+    hX, hW, hdY = (t.cpu().pin_memory() for t in (X, W, dY))
+    hY, hdX, hdW = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (b["Y"], b["dX"], b["dW"]))
+    h2d = sum(t.numel() * t.element_size() for t in (hX, hW, hdY))
+    d2h = sum(t.numel() * t.element_size() for t in (hY, hdX, hdW))
+    # uploads in the order dY, X, W: the longest quantization (dY, stochastic
+    # rounding) overlaps the uploads after it; each compute step waits for its
+    # own input's upload; each GEMM's download overlaps the GEMMs after it
+    copy_stream = torch.cuda.Stream(dev)
+    e2e_q, e2e_g = [], []
+    warm = max(args.warmup, 10)
+    for it in range(warm + args.steps):
+        flush.zero_()
+        e0, e1, e2 = ev(), ev(), ev()
+        e0.record(stream)
+        copy_stream.wait_event(e0)
+        up = [ev() for _ in range(3)]
+        with torch.cuda.stream(copy_stream):
+            for dst, src, u in ((dY, hdY, up[0]), (X, hX, up[1]), (W, hW, up[2])):
+                dst.copy_(src, non_blocking=True)
+                u.record(copy_stream)
+        for u, (x, cfg, ro, co) in zip(up, ((dY, cg, b["Gr"], b["Gc"]), (X, cx, b["Xr"], b["Xc"]),
+                                            (W, cw, b["Wr"], b["Wc"]))):
+            stream.wait_event(u)
+            fp4q.rht_quantize(x, cfg, ro, co, status=status, stream=stream)
+        e1.record(stream)
+        fp4q.gemm(b["Xr"], b["Wr"], b["grid"], fp4q.SCALE_MX, want_f32=False, D_bf16=b["Y"], status=status,
+                  stream=stream)
+        g = ev()
+        g.record(stream)
+        copy_stream.wait_event(g)
+        with torch.cuda.stream(copy_stream):
+            hY.copy_(b["Y"], non_blocking=True)
+        fp4q.gemm_group([(b["Gr"], b["Wc"]), (b["Gc"], b["Xc"])], b["grid"], fp4q.SCALE_MX, want_bf16=True,
+                        want_f32=False, outs=[(b["dX"], None), (b["dW"], None)], status=status, stream=stream)
+        g = ev()
+        g.record(stream)
+        copy_stream.wait_event(g)
+        with torch.cuda.stream(copy_stream):
+            hdX.copy_(b["dX"], non_blocking=True)
+            hdW.copy_(b["dW"], non_blocking=True)
+        down = ev()
+        down.record(copy_stream)
+        stream.wait_event(down)
+        e2.record(stream)
+        e2.synchronize()
+        if it >= warm:
+            e2e_q.append(e0.elapsed_time(e1) * 1e-3)
+            e2e_g.append(e1.elapsed_time(e2) * 1e-3)
+    q_med, g_med = statistics.median(e2e_q), statistics.median(e2e_g)
+    e2e_value = aggregate(q_bytes, q_med, world, dev) / 1e9
+    e2e_gemm = aggregate(flops, g_med, world, dev) / 1e12
+    # the link alone: the same uploads and downloads with no compute (median of 5)
+    link = {}
+    for name, pairs in (("h2d", ((dY, hdY), (X, hX), (W, hW))), ("d2h", ((hY, b["Y"]), (hdX, b["dX"]),
+                                                                      (hdW, b["dW"])))):
+        ts = []
+        for _ in range(5):
+            a, z = ev(), ev()
+            a.record(copy_stream)
+            with torch.cuda.stream(copy_stream):
+                for dst, src in pairs:
+                    dst.copy_(src, non_blocking=True)
+            z.record(copy_stream)
+            z.synchronize()
+            ts.append(a.elapsed_time(z) * 1e-3)
+        link[name] = (h2d if name == "h2d" else d2h) / sorted(ts)[2] / 1e9
+    return {"value": round(e2e_value, 1), "unit": "GB/s", "gemm_tflops": round(e2e_gemm, 1),
+            "statistic": f"median of {args.steps} steps after {warm} untimed ones",
+            "quantize_spread": pct(e2e_q), "gemm_spread": pct(e2e_g),
+            "quantize_mean_us": round(statistics.mean(e2e_q) * 1e6, 2),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "link_h2d_gb_s": round(link["h2d"], 1), "link_d2h_gb_s": round(link["d2h"], 1),
+            "note": "H2D of dY/X/W (in that order) inside the quantize phase, D2H of Y/dX/dW inside the GEMM "
+                    "phase; copies on a second stream overlap the compute that does not depend on them; "
+                    "link_*: the same copies alone"}
+
+
+def tiny_config(dev, stream) -> dict:
+    """The tiny single-tensor workload (X 256x512, N(0,1) with 1% of positions
+    x50; row-wise copy, H16 with seeded signs, MX E2M1 and E1M2, RTNE): the
+    codes and scales (SHA-256 and code histogram), and the reconstruction's
+    SQNR, attenuation alpha and shrinkage against X in the original domain."""
+    import torch
+
+    from fp4_microscaled_quantization_gb300 import fp4q, synth
+    bits = synth.tiny_x()
+    x = synth.as_torch(bits).to(dev)
+    xf = x.float()
+    mask = fp4q.sign_mask_from_seed(1001, 16)
+    out = {"shape": "256x512", "rot": "H16", "sign_mask": f"{mask:#06x}"}
+    for g, name in ((0, "e2m1"), (1, "e1m2")):
+        cfg = fp4q.Config(grid=g, rot=16, sign_mask_row=mask, want_col=False)
+        ro, _ = fp4q.rht_quantize(x, cfg, stream=stream)
+        deq = fp4q.dequantize(ro, cfg, orient=0, unrotate=True)
+        st = fp4q.bias_stats(xf, deq, ro.codes)
+        torch.cuda.synchronize(dev)
+        codes = ro.codes.cpu().numpy()
+        scales = ro.scales.cpu().numpy()
+        out[name] = {"codes_sha256": synth.sha256(codes), "scales_sha256": synth.sha256(scales),
+                     "code_histogram": [int(v) for v in st["hist"]],
+                     "sqnr_db": round(st["sqnr_db"], 4), "alpha": round(st["alpha"], 6),
+                     "shrinkage": round(st["shrinkage"], 6)}
+    return out
 
 
 def read_traffic() -> dict:
@@ -570,7 +701,8 @@ def cpu_baseline(args, rows: int = 1024, min_s: float = 10.0) -> dict:
         if time.perf_counter() - t0 >= min_s:
             break
     dt = (time.perf_counter() - t0) / n
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "cpu_model": cpu_model(),
+            "host_threads": os.cpu_count(), "kind": "oracle",
             "sample": f"quantize (both copies) of rows 0..{rows - 1} of X and dY and rows 0..{Ws.shape[0] - 1} "
                       f"of W of the same workload, {n} repetitions, {dt:.2f} s each; GEMMs not included"}
 
@@ -598,7 +730,8 @@ def run_reference(args, world, rank):
             "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "fp32 quantizer arithmetic (CPU oracle)", "data": "synthetic (seeded)",
             "config": {"workload": WORKLOAD, "sample": sample},
-            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "cpu_model": cpu_model(), "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

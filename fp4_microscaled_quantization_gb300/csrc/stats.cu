@@ -4,12 +4,15 @@
 // Metodologia 1 "Impacto Sistemico"; Resultados, quantization diagnostics),
 // plus a histogram of the packed 4-bit codes (codebook use).
 //
-// HBM-bound streaming reduction.  The grid is fixed (a multiple of the SM
-// count), every thread accumulates a grid-stride slice in fp64, CTAs reduce
-// in a fixed tree and the last CTA to finish sums the per-CTA partials in CTA
-// order, so results are bit-reproducible run to run.
+// HBM-bound streaming reduction.  The grid is four CTAs per SM of the device
+// (at most kStatsMaxBlocks), every thread accumulates a grid-stride slice in
+// fp64, CTAs reduce in a fixed tree and the last CTA to finish sums the
+// per-CTA partials in CTA order, so results are bit-reproducible run to run
+// on a given device.
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <atomic>
 
 #include "fp4q_dev.cuh"
 #include "fp4q_internal.h"
@@ -17,19 +20,24 @@
 namespace fp4q {
 
 constexpr int kStatsThreads = 256;
-constexpr int kStatsBlocks = 152 * 4;
+constexpr int kStatsMaxBlocks = 640;   // workspace bound: four CTAs per SM up to 160 SMs
 constexpr int kSums = 5;
 
-// Workspace: [kStatsBlocks][kSums] doubles, [kStatsBlocks][16] uint64 histogram
-// partials, then one uint32 arrival counter.
+int stats_blocks() {
+  const int b = 4 * num_sms();
+  return b < kStatsMaxBlocks ? b : kStatsMaxBlocks;
+}
+
+// Workspace: [kStatsMaxBlocks][kSums] doubles, [kStatsMaxBlocks][16] uint64
+// histogram partials, then one uint32 arrival counter.
 size_t bias_stats_workspace(int64_t /*n*/) {
-  return (size_t)kStatsBlocks * (kSums + 16) * 8 + 256;
+  return (size_t)kStatsMaxBlocks * (kSums + 16) * 8 + 256;
 }
 
 __global__ void __launch_bounds__(kStatsThreads) bias_stats_kernel(StatsParams sp) {
   double* part = reinterpret_cast<double*>(sp.workspace);
-  unsigned long long* hpart = reinterpret_cast<unsigned long long*>(part + kStatsBlocks * kSums);
-  unsigned int* counter = reinterpret_cast<unsigned int*>(hpart + kStatsBlocks * 16);
+  unsigned long long* hpart = reinterpret_cast<unsigned long long*>(part + kStatsMaxBlocks * kSums);
+  unsigned int* counter = reinterpret_cast<unsigned int*>(hpart + kStatsMaxBlocks * 16);
   __shared__ double red[kSums][kStatsThreads / 32];
   __shared__ unsigned int hist[16];
   __shared__ bool last;
@@ -111,9 +119,9 @@ __global__ void __launch_bounds__(kStatsThreads) bias_stats_kernel(StatsParams s
 
 cudaError_t launch_bias_stats(const StatsParams& sp, cudaStream_t s) {
   unsigned char* ws = reinterpret_cast<unsigned char*>(sp.workspace);
-  cudaError_t e = cudaMemsetAsync(ws + (size_t)kStatsBlocks * (kSums + 16) * 8, 0, 4, s);
+  cudaError_t e = cudaMemsetAsync(ws + (size_t)kStatsMaxBlocks * (kSums + 16) * 8, 0, 4, s);
   if (e != cudaSuccess) return e;
-  bias_stats_kernel<<<kStatsBlocks, kStatsThreads, 0, s>>>(sp);
+  bias_stats_kernel<<<stats_blocks(), kStatsThreads, 0, s>>>(sp);
   return cudaGetLastError();
 }
 
@@ -127,8 +135,12 @@ cudaError_t launch_bias_stats(const StatsParams& sp, cudaStream_t s) {
 // workspace, so a caller that may not allocate device memory can still run
 // it.  Every GPU that loads the library keeps the array until the process
 // exits.  Its device address is looked up once per device (the first call on
-// that device, with the device current) and cached; in host code the symbol is
-// only a host-side stand-in and must never be handed to a kernel directly.
+// that device, with the device current) and cached in an atomic per device, so
+// concurrent first calls from several host threads are safe; after
+// cudaDeviceReset the module is loaded again and the address may change, so a
+// reset must be followed by fp4q_bias_stats_noalloc_reset().  In host code the
+// symbol is only a host-side stand-in and must never be handed to a kernel
+// directly.
 // All calls share the array: the counter is cleared on every call and the
 // partials are overwritten, but two calls that overlap on the GPU (different
 // streams, or different host threads) race on it.
@@ -137,8 +149,12 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = 128 * 1024;
 constexpr int kMaxDevices = 64;
 __device__ __align__(256) unsigned char g_stats_scratch[kNoAllocScratchBytes];
-void* g_scratch_addr[kMaxDevices] = {};
+std::atomic<void*> g_scratch_addr[kMaxDevices];
 }  // namespace
+
+extern "C" void fp4q_bias_stats_noalloc_reset(void) {
+  for (int d = 0; d < kMaxDevices; ++d) g_scratch_addr[d].store(nullptr, std::memory_order_release);
+}
 
 extern "C" int32_t fp4q_bias_stats_noalloc(const float* ref, const float* approx, int64_t n,
                                            const uint8_t* codes, void* out, void* stream) {
@@ -153,17 +169,17 @@ extern "C" int32_t fp4q_bias_stats_noalloc(const float* ref, const float* approx
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FP4Q_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return FP4Q_ERR_UNSUPPORTED;
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_stats_scratch) != cudaSuccess || !p) return FP4Q_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+  void* scratch = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (!scratch) {
+    if (cudaGetSymbolAddress(&scratch, g_stats_scratch) != cudaSuccess || !scratch) return FP4Q_ERR_CUDA;
+    g_scratch_addr[dev].store(scratch, std::memory_order_release);   // every thread stores the same address
   }
   StatsParams sp;
   sp.ref = ref;
   sp.approx = approx;
   sp.codes = codes;
   sp.n = n;
-  sp.workspace = g_scratch_addr[dev];
+  sp.workspace = scratch;
   sp.out = out;
   return launch_bias_stats(sp, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FP4Q_OK : FP4Q_ERR_CUDA;
 }

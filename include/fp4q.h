@@ -256,15 +256,21 @@ int32_t fp4q_bias_stats(const float* ref, const float* approx, int64_t n, const 
  * exits).  Same arguments, results and determinism as fp4q_bias_stats.
  *  - Calls whose scratch need (fp4q_bias_stats_workspace_bytes(n)) exceeds the
  *    built-in 128 KiB return FP4Q_ERR_WORKSPACE; the current reduction needs
- *    about 100 KiB for every n, so every n >= 0 fits.
+ *    about 105 KiB for every n, so every n >= 0 fits.
  *  - The first call on each device looks up the array's device address (with
- *    that device current) and caches it; make that first call before any
- *    stream capture.
+ *    that device current) and caches it (safe when several host threads make
+ *    that first call at once); make that first call before any stream
+ *    capture.  After cudaDeviceReset the library's device array is loaded
+ *    anew: call fp4q_bias_stats_noalloc_reset() so that the next call looks
+ *    the address up again.
  *  - All calls share the one array: two calls that overlap on the GPU (other
  *    streams, other host threads) race and give undefined sums.
  *  - It calls no cudaMalloc, cudaFree or other allocating routine. */
 int32_t fp4q_bias_stats_noalloc(const float* ref, const float* approx, int64_t n, const uint8_t* codes,
                                 void* out, void* stream);
+/* Forget the cached device addresses of that array (host only; after a
+ * device reset). */
+void fp4q_bias_stats_noalloc_reset(void);
 
 /* Host helper: SQNR (dB), alpha and shrinkage from the five sums above. */
 void fp4q_stats_finalize(const double* sums5, double* sqnr_db, double* alpha, double* shrinkage);
