@@ -79,6 +79,8 @@ int32_t prepare(const void* x, int64_t rows, int64_t cols, int64_t ld, const fp4
   p.emit_e4m3 = cfg->emit_e4m3 ? 1 : 0;
   sign_words(cfg->sign_mask_row, cfg->rot, p.sgn_row);
   sign_words(cfg->sign_mask_col, cfg->rot, p.sgn_col);
+  p.stall_tile = -1;
+  p.wait_limit_ns = 0;
   return FP4Q_OK;
 }
 
@@ -114,9 +116,14 @@ size_t fp4q_workspace_bytes(int64_t rows, int64_t cols, const fp4q_config* cfg) 
   return (cfg->scale == FP4Q_SCALE_NV && cfg->global_amax == nullptr) ? 256 : 0;
 }
 
-int32_t fp4q_rht_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, const fp4q_config* cfg,
+}  // extern "C"
+
+namespace {
+// fp4q_rht_quantize with the bounded-wait test parameters (stall_tile < 0: none).
+int32_t rht_quantize_impl(const void* x, int64_t rows, int64_t cols, int64_t ld, const fp4q_config* cfg,
                           const fp4q_operand* row_out, const fp4q_operand* col_out, void* workspace,
-                          size_t ws_bytes, uint32_t* d_status, void* stream) {
+                          size_t ws_bytes, uint32_t* d_status, void* stream, int32_t stall_tile,
+                          uint32_t wait_limit_ns) {
   QuantParams p;
   int32_t st = prepare(x, rows, cols, ld, cfg, p);
   if (st != FP4Q_OK || rows == 0 || cols == 0) return st;
@@ -142,7 +149,28 @@ int32_t fp4q_rht_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld,
       p.gamax = g;
     }
   }
+  p.stall_tile = stall_tile;
+  p.wait_limit_ns = wait_limit_ns;
   return cuda_status(launch_rht_quant(p, cfg->grid, cfg->scale, cfg->rot, cfg->round, s));
+}
+}  // namespace
+
+extern "C" {
+
+int32_t fp4q_rht_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, const fp4q_config* cfg,
+                          const fp4q_operand* row_out, const fp4q_operand* col_out, void* workspace,
+                          size_t ws_bytes, uint32_t* d_status, void* stream) {
+  return rht_quantize_impl(x, rows, cols, ld, cfg, row_out, col_out, workspace, ws_bytes, d_status, stream, -1, 0);
+}
+
+int32_t fp4q_test_quantize_wait_expiry(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                       const fp4q_config* cfg, const fp4q_operand* row_out,
+                                       const fp4q_operand* col_out, void* workspace, size_t ws_bytes,
+                                       uint32_t* d_status, int32_t stall_tile, uint32_t wait_limit_us,
+                                       void* stream) {
+  if (stall_tile < 0 || wait_limit_us == 0 || wait_limit_us > 2000000u) return FP4Q_ERR_INVALID_ARG;
+  return rht_quantize_impl(x, rows, cols, ld, cfg, row_out, col_out, workspace, ws_bytes, d_status, stream,
+                           stall_tile, wait_limit_us * 1000u);
 }
 
 int32_t fp4q_rotated_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, const fp4q_config* cfg,

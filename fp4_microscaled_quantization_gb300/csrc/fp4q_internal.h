@@ -29,6 +29,11 @@ struct QuantParams {
   int32_t want_row, want_col, sf_mma, emit_e4m3;
   uint32_t sgn_row[32];  // bit 31 set: negate element t of a 32-element chunk (row-wise)
   uint32_t sgn_col[32];  // same, column-wise copy
+  // Bounded-wait test (fp4q_test_quantize_wait_expiry only; 0 / -1 otherwise):
+  // CTA 0 waits for its tile stall_tile on a barrier nothing arrives at, giving
+  // up after wait_limit_ns instead of the usual ~2 s.
+  int32_t stall_tile;
+  uint32_t wait_limit_ns;
 };
 
 // 2-D tensor map (inner dimension contiguous) and the device's SM count.

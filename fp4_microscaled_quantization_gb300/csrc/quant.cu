@@ -80,7 +80,7 @@ __device__ __forceinline__ void store_chunk(const CopyOut& d, int64_t r, int64_t
 constexpr int kStages = QUANT_STAGES;              // tiles in flight per CTA
 constexpr int kBoxBytes = kTR * 128;               // one 64-column box
 constexpr int kTileBytes = kTR * kTC * 2;          // 16 KB
-constexpr int kQuantSmem = kStages * kTileBytes + 1024 + 64;
+constexpr int kQuantSmem = kStages * kTileBytes + 1024 + 64;   // tiles, alignment, barriers
 
 struct TileView {
   const uint8_t* t;
@@ -104,8 +104,10 @@ __device__ __forceinline__ bool mbar_done(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for a phase of an mbarrier, giving up after about 2 s.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Wait for a phase of an mbarrier, giving up after limit_ns (about 2 s by
+// default).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns = 2000000000ull) {
   uint64_t t0 = 0;
   for (uint32_t i = 0;; ++i) {
     if (mbar_done(bar, parity)) return true;
@@ -113,7 +115,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
       uint64_t now;
       asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
       if (t0 == 0) t0 = now;
-      else if (now - t0 > 2000000000ull) return false;
+      else if (now - t0 > limit_ns) return false;
     }
   }
 }
@@ -128,6 +130,8 @@ struct TileRing {
   uint32_t bar0;
   int ntc, ntiles;
   const CUtensorMap* tm;
+  int stall_tile;          // bounded-wait test: CTA 0's tile that waits on bar_never
+  uint64_t stall_limit_ns;
 
   __device__ __forceinline__ void issue(int s, int tile) const {
     const int tr0 = (tile / ntc) * kTR, tc0 = (tile % ntc) * kTC;
@@ -141,15 +145,19 @@ struct TileRing {
           : "memory");
   }
 
-  __device__ __forceinline__ void init(const CUtensorMap* tmap, int64_t rows, int64_t cols) {
+  __device__ __forceinline__ void init(const CUtensorMap* tmap, int64_t rows, int64_t cols,
+                                      int stall = -1, uint32_t stall_ns = 0) {
     extern __shared__ uint8_t smem_raw[];
     smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     bar0 = smem_addr(smem + kStages * kTileBytes);
     ntc = (int)((cols + kTC - 1) / kTC);
     ntiles = ntc * (int)((rows + kTR - 1) / kTR);
     tm = tmap;
+    stall_tile = blockIdx.x == 0 ? stall : -1;
+    stall_limit_ns = stall_ns;
     if (threadIdx.x == 0) {
-      for (int s = 0; s < kStages; ++s)
+      // kStages tile barriers, then one that nothing ever arrives at
+      for (int s = 0; s <= kStages; ++s)
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8 * s) : "memory");
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -167,7 +175,8 @@ struct TileRing {
   // and draining this CTA's own loads) when it did not arrive in time.
   __device__ __forceinline__ bool wait(int k, uint32_t* status) const {
     const int s = k % kStages;
-    const bool ok = mbar_wait_bounded(bar0 + 8 * s, (uint32_t)(k / kStages) & 1u);
+    const bool ok = k == stall_tile ? mbar_wait_bounded(bar0 + 8 * kStages, 0u, stall_limit_ns)
+                                    : mbar_wait_bounded(bar0 + 8 * s, (uint32_t)(k / kStages) & 1u);
     if (__syncthreads_or(!ok)) {
       if (threadIdx.x == 0) {
         raise_status(status, FP4Q_DEV_TIMEOUT);
@@ -260,7 +269,7 @@ __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
     }
   }
   TileRing ring;
-  ring.init(&tmx, p.rows, p.cols);
+  ring.init(&tmx, p.rows, p.cols, p.stall_tile, p.wait_limit_ns);
   int k = 0;
   for (int tile = blockIdx.x; tile < ring.ntiles; tile += gridDim.x, ++k) {
     if (!ring.wait(k, p.status)) return;

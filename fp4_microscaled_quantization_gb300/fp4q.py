@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
         L.fp4q_workspace_bytes.argtypes = [i64, i64, P]
         L.fp4q_rht_quantize.restype = i32
         L.fp4q_rht_quantize.argtypes = [P, i64, i64, i64, P, P, P, P, sz, P, P]
+        L.fp4q_test_quantize_wait_expiry.restype = i32
+        L.fp4q_test_quantize_wait_expiry.argtypes = [P, i64, i64, i64, P, P, P, P, sz, P, i32, u32, P]
         L.fp4q_rotated_amax.restype = i32
         L.fp4q_rotated_amax.argtypes = [P, i64, i64, i64, P, P, P, P]
         L.fp4q_dequantize.restype = i32
@@ -207,6 +209,23 @@ def rht_quantize(x: torch.Tensor, cfg: Config, row_out: Operand | None = None, c
         _p(workspace), 0 if workspace is None else workspace.numel(), _p(status), _stream(stream))
     _check("fp4q_rht_quantize", s)
     return (row_out if cfg.want_row else None), (col_out if cfg.want_col else None)
+
+
+def test_quantize_wait_expiry(x: torch.Tensor, cfg: Config, row_out: Operand, col_out: Operand | None,
+                              status: torch.Tensor, stall_tile: int, wait_limit_us: int, stream=None):
+    """fp4q_test_quantize_wait_expiry: fp4q_rht_quantize with CTA 0's wait for
+    its tile stall_tile made to run out after wait_limit_us (tests the bounded
+    waits; FP4Q_DEV_TIMEOUT is expected in `status`)."""
+    R, C = x.shape
+    need = workspace_bytes(R, C, cfg)
+    workspace = torch.empty(need, dtype=torch.uint8, device=x.device) if need else None
+    cc = cfg.c()
+    ro = row_out.c() if cfg.want_row else None
+    co = col_out.c() if cfg.want_col else None
+    _check("fp4q_test_quantize_wait_expiry", lib().fp4q_test_quantize_wait_expiry(
+        x.data_ptr(), R, C, x.stride(0), ctypes.byref(cc), ctypes.byref(ro) if ro is not None else None,
+        ctypes.byref(co) if co is not None else None, _p(workspace), 0 if workspace is None else workspace.numel(),
+        _p(status), stall_tile, wait_limit_us, _stream(stream)))
 
 
 def rotated_amax(x: torch.Tensor, cfg: Config, out: torch.Tensor | None = None, status=None, stream=None):

@@ -275,6 +275,22 @@ void fp4q_bias_stats_noalloc_reset(void);
 /* Host helper: SQNR (dB), alpha and shrinkage from the five sums above. */
 void fp4q_stats_finalize(const double* sums5, double* sqnr_db, double* alpha, double* shrinkage);
 
+/* Test of the quantizer's bounded waits (no page counterpart): the same call
+ * as fp4q_rht_quantize, except that CTA 0 waits for its tile number
+ * stall_tile (0 = its first tile) on a pipeline barrier that nothing arrives
+ * at, and gives up after wait_limit_us microseconds (1 .. 2000000) instead of
+ * the usual ~2 s.  That CTA then raises FP4Q_DEV_TIMEOUT in *d_status, waits
+ * (bounded) for its own tile loads in flight and returns, leaving its tiles
+ * unwritten; the other CTAs finish normally and the context stays usable.
+ * A stall_tile past CTA 0's last tile changes nothing.  Returns
+ * FP4Q_ERR_INVALID_ARG for stall_tile < 0 or a limit outside that range,
+ * otherwise as fp4q_rht_quantize. */
+int32_t fp4q_test_quantize_wait_expiry(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                                       const fp4q_config* cfg, const fp4q_operand* row_out,
+                                       const fp4q_operand* col_out, void* workspace, size_t ws_bytes,
+                                       uint32_t* d_status, int32_t stall_tile, uint32_t wait_limit_us,
+                                       void* stream);
+
 /* Unfused comparison arm (measurement only, [SB] Eficiencia: fused versus
  * unfused rotation + quantization): rotate x blockwise along its rows
  * (orient 0) or columns (orient 1) and write the rotated tensor in bf16
