@@ -9,7 +9,8 @@ numpy's fp64 matrix product as a library step.
 
 Parity status of each function (pins live in tests/test_oracle_*.py):
   grid tables, E4M3 codec, Philox4x32-10, rotation, RTNE, SR, MX and NV
-  scales, dequantize, GEMM entries, bias sums, effective bucket ratio -- pinned.
+  scales, dequantize, GEMM entries, bias sums, effective bucket ratio, the
+  per-level error in grid units and the per-element relative error -- pinned.
 """
 from __future__ import annotations
 
@@ -88,6 +89,10 @@ def lib() -> ctypes.CDLL:
         L.orc_gemm_entries.argtypes = [P, P, i64, ctypes.c_double, P, P, i64, P]
         L.orc_bias_sums.restype = None
         L.orc_bias_sums.argtypes = [P, P, i64, P, P, P]
+        L.orc_grid_error.restype = None
+        L.orc_grid_error.argtypes = [P, i64, i64, i64, i32, i32, i32, u32, P, P, ctypes.c_float, P, P]
+        L.orc_rel_error_sums.restype = None
+        L.orc_rel_error_sums.argtypes = [P, P, i64, P]
         _lib = L
     return _lib
 
@@ -234,6 +239,32 @@ def bias_stats(ref: np.ndarray, approx: np.ndarray, codes: np.ndarray | None = N
     alpha = s_ra / s_ref2 if s_ref2 > 0 else float("nan")
     shrink = s_absdiff / s_absref if s_absref > 0 else float("nan")
     return {"sums": sums, "hist": hist, "n": r.size, "sqnr_db": sqnr, "alpha": alpha, "shrinkage": shrink}
+
+
+def grid_error(x_bf16: np.ndarray, grid: int, scale: int, n_h: int, sign_mask: int, codes: np.ndarray,
+               scales: np.ndarray, tensor_scale: float = 0.0) -> dict:
+    """Per level k: sum and count of g[k] - |v| (v in grid units) over the
+    row-wise copy (plain scales) of x; the mean over all elements."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    R, C = x.shape
+    sums = np.zeros(8, dtype=np.float64)
+    counts = np.zeros(8, dtype=np.uint64)
+    lib().orc_grid_error(_ptr(x), R, C, C, grid, scale, n_h, sign_mask,
+                         _ptr(np.ascontiguousarray(codes, dtype=np.uint8)),
+                         _ptr(np.ascontiguousarray(scales, dtype=np.uint8)), float(tensor_scale),
+                         _ptr(sums), _ptr(counts))
+    total = int(counts.sum())
+    return {"sums": sums, "counts": counts, "mean": float(sums.sum() / total) if total else float("nan")}
+
+
+def rel_error(ref: np.ndarray, approx: np.ndarray) -> dict:
+    """Mean of (|approx| - |ref|) / |ref| over ref != 0 (fp64 sums)."""
+    r = np.ascontiguousarray(ref, dtype=np.float32).ravel()
+    a = np.ascontiguousarray(approx, dtype=np.float32).ravel()
+    sums = np.zeros(2, dtype=np.float64)
+    lib().orc_rel_error_sums(_ptr(r), _ptr(a), r.size, _ptr(sums))
+    return {"sum": float(sums[0]), "count": int(sums[1]),
+            "mean": float(sums[0] / sums[1]) if sums[1] else float("nan")}
 
 
 def effective_bucket_ratio(hist16, grid: int) -> float:

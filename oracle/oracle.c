@@ -539,3 +539,71 @@ void orc_bias_sums(const float *ref, const float *approx, int64_t n,
             for (int64_t t = 0; t < n; ++t) hist[(codes[t >> 1] >> ((t & 1) * 4)) & 15] += 1;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Rounding error in grid units, per level ([SB] Metodologia 1, "Origem      */
+/* Geometrica": the expected error of the elements that round to level q_i, */
+/* (l_i - r_i)/2 under a uniform density, is negative where the level's bin  */
+/* is wider above it than below).                                          */
+/* ------------------------------------------------------------------------ */
+/* For the row-wise copy (codes, plain scales, tensor scale) of the R x C bf16
+ * matrix x: every element's position v = y * step^-1 in grid units (y the
+ * rotated value, the element step exactly as orc_quantize computes it), its
+ * code's level g[k], k = code & 7, and per level k the sum of g[k] - |v| in
+ * fp64 (sums[k]) and the number of elements (counts[k]).  Elements of a block
+ * whose NV scale byte is 0 have v = 0. */
+void orc_grid_error(const uint16_t *x, int64_t R, int64_t C, int64_t ld, int grid, int scale, int n_h,
+                    uint32_t sign_mask, const uint8_t *codes, const uint8_t *scales, float tensor_scale,
+                    double *sums, uint64_t *counts)
+{
+    int b = (scale == ORC_SCALE_MX) ? 32 : 16;
+    int64_t nblk = C / b;
+    float *y = (float *)malloc(sizeof(float) * (size_t)(C > 0 ? C : 1));
+    if (!y) return;
+    for (int k = 0; k < 8; ++k) { sums[k] = 0.0; counts[k] = 0; }
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t j = 0; j < C; ++j) y[j] = orc_bf16_to_f32(x[r * ld + j]);
+        if (n_h)
+            for (int64_t j0 = 0; j0 < C; j0 += n_h) orc_rotate_block(&y[j0], n_h, sign_mask);
+        for (int64_t kb = 0; kb < nblk; ++kb) {
+            uint8_t sb = scales[r * nblk + kb];
+            float vmul;
+            if (scale == ORC_SCALE_MX) {
+                vmul = ldexpf(1.0f, 127 - (int)sb);
+            } else if (sb == 0 || !(tensor_scale > 0.0f)) {
+                vmul = 0.0f;
+            } else {
+                float d = orc_e4m3_decode(sb) * tensor_scale;
+                vmul = 1.0f / d;
+                if (isinf(vmul)) vmul = FLT_MAX;
+            }
+            for (int t = 0; t < b; ++t) {
+                int64_t idx = r * C + kb * b + t;
+                int code = (codes[idx >> 1] >> ((idx & 1) * 4)) & 15;
+                float v = y[kb * b + t] * vmul;
+                int k = code & 7;
+                sums[k] += (double)orc_grid_level(grid, k) - fabs((double)v);
+                counts[k] += 1;
+            }
+        }
+    }
+    free(y);
+}
+
+/* Mean signed relative error of approx against ref over the elements with
+ * ref != 0: sums[0] = sum (|approx| - |ref|) / |ref| (each term in fp64),
+ * sums[1] = their number.  The per-element form of the shrinkage, reported
+ * beside the aggregate sum(|approx| - |ref|) / sum |ref|. */
+void orc_rel_error_sums(const float *ref, const float *approx, int64_t n, double *sums)
+{
+    double s = 0.0, c = 0.0;
+    for (int64_t t = 0; t < n; ++t) {
+        double r = ref[t], a = approx[t];
+        if (r != 0.0) {
+            s += (fabs(a) - fabs(r)) / fabs(r);
+            c += 1.0;
+        }
+    }
+    sums[0] = s;
+    sums[1] = c;
+}

@@ -135,3 +135,83 @@ def test_effective_bucket_ratio_of_quantized_uniform_data(orc):
                         q["codes"])
     assert st["sqnr_db"] == float("inf")
     assert orc.effective_bucket_ratio(st["hist"], orc.GRID_E1M2) == pytest.approx(1.0, abs=1e-15)
+
+
+def test_rel_error_hand_example(orc):
+    """Per-element mean signed relative error over ref != 0, against the hand
+    value in the golden file; elements with ref = 0 are left out."""
+    g = _golden_stats()
+    s = orc.rel_error(np.array(g["ref"], np.float32), np.array(g["approx"], np.float32))
+    assert s["mean"] == g["mean_rel_error"][0] and s["count"] == 2
+    s0 = orc.rel_error(np.array(g["ref"] + [0.0], np.float32), np.array(g["approx"] + [5.0], np.float32))
+    assert s0["mean"] == g["mean_rel_error"][0] and s0["count"] == 2
+
+
+def _bin_midpoints(lo, hi, w):
+    """Midpoints of the strata of width w that tile [lo, hi)."""
+    n = int(round((hi - lo) / w))
+    return lo + (np.arange(n) + 0.5) * w
+
+
+# (grid, level, RTNE bin of the level, stratum width, block maximum in another level)
+_BIN_CASES = [(0, 2.0, (1.75, 2.5), 1 / 32, 6.0), (0, 4.0, (3.5, 5.0), 1 / 16, 6.0),
+              (0, 1.5, (1.25, 1.75), 1 / 32, 6.0), (0, 3.0, (2.5, 3.5), 1 / 32, 6.0),
+              (1, 0.75, (0.625, 0.875), 1 / 128, 1.75), (1, 1.25, (1.125, 1.375), 1 / 64, 1.75)]
+
+
+@pytest.mark.parametrize("grid,level,bin_,w,vmax", _BIN_CASES)
+def test_grid_error_per_level_equals_half_bin_asymmetry(orc, grid, level, bin_, w, vmax):
+    """Inputs spread evenly over one level's RTNE bin (stratum midpoints, all
+    exact in bf16), one block maximum in another level so that the block scale
+    is 1: the level's mean error in grid units is the page's (l_i - r_i)/2
+    (golden, "Repensando o Vies de Encolhimento", Metodologia 1), exactly,
+    since the error is linear in x within the bin."""
+    want = {(g, lvl): w_ for g, lvl, w_ in _golden_cond_error()}[(grid, level)]
+    vals = _bin_midpoints(*bin_, w).astype(np.float32)
+    per_block = 16
+    nb = (vals.size + per_block - 1) // per_block
+    x = np.zeros((1, 32 * nb), np.float32)
+    for b in range(nb):
+        part = vals[b * per_block:(b + 1) * per_block]
+        x[0, 32 * b] = vmax
+        x[0, 32 * b + 1:32 * b + 1 + part.size] = part
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal((bits.astype(np.uint32) << 16).view(np.float32), x)   # exact in bf16
+    q = orc.quantize(bits, 0, grid, orc.SCALE_MX, 0)
+    assert np.all(q["scales"] == 127)
+    ge = orc.grid_error(bits, grid, orc.SCALE_MX, 0, 0, q["codes"], q["scales"])
+    k = int(np.where(orc.grid_levels(grid) == np.float32(level))[0][0])
+    assert int(ge["counts"][k]) == vals.size
+    assert ge["sums"][k] / ge["counts"][k] == want
+
+
+def _golden_cond_error():
+    out = []
+    for line in open(os.path.join(GOLDEN, "conditional_error.txt")):
+        if line.strip() and not line.startswith("#"):
+            g, lvl, want = line.split()
+            out.append(({"e2m1": 0, "e1m2": 1, "e2m1r4": 2}[g], float(lvl), float(want)))
+    return out
+
+
+@pytest.mark.parametrize("grid,scale,rot", [(0, 0, 16), (1, 0, 32), (0, 1, 16), (2, 0, 0)])
+def test_grid_error_within_each_bin(orc, grid, scale, rot):
+    """Every element's error in grid units lies within its level's RTNE bin
+    (-r_i <= g - |v| <= l_i, saturated elements below -r only), on rotated
+    random data with MX and NVFP4-style scales; zero blocks count at level 0."""
+    bits = synth.normal_channel_outliers(64, 256, 77, 4, 30.0)
+    bits[:, 32:64] = 0
+    q = orc.quantize(bits, 0, grid, scale, rot, 0x2A5B)
+    ge = orc.grid_error(bits, grid, scale, rot, 0x2A5B, q["codes"], q["scales"], q["tensor_scale"])
+    L = orc.grid_levels(grid).astype(np.float64)
+    top = orc.grid_top(grid)
+    assert int(ge["counts"].sum()) == bits.size
+    for k in range(top + 1):
+        if ge["counts"][k] == 0:
+            continue
+        left = (L[k] - L[k - 1]) / 2 if k > 0 else 0.0
+        mean = ge["sums"][k] / ge["counts"][k]
+        assert mean <= left + 1e-12, (k, mean)
+        if k < top:
+            right = (L[k + 1] - L[k]) / 2
+            assert mean >= -right - 1e-12, (k, mean)
