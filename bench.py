@@ -482,7 +482,9 @@ def tiny_config(dev, stream) -> dict:
     """The tiny single-tensor workload (X 256x512, N(0,1) with 1% of positions
     x50; row-wise copy, H16 with seeded signs, MX E2M1 and E1M2, RTNE): the
     codes and scales (SHA-256 and code histogram), and the reconstruction's
-    SQNR, attenuation alpha and shrinkage against X in the original domain."""
+    SQNR, attenuation alpha and shrinkage against X in the original domain,
+    the per-element mean signed relative error beside that aggregate, and the
+    rounding error in grid units, overall and per level."""
     import torch
 
     from fp4_microscaled_quantization_gb300 import fp4q, synth
@@ -496,13 +498,19 @@ def tiny_config(dev, stream) -> dict:
         ro, _ = fp4q.rht_quantize(x, cfg, stream=stream)
         deq = fp4q.dequantize(ro, cfg, orient=0, unrotate=True)
         st = fp4q.bias_stats(xf, deq, ro.codes)
+        rel = fp4q.rel_error(xf.reshape(-1), deq.reshape(-1), stream=stream)
+        ge = fp4q.grid_error(x, cfg, ro, stream=stream)
         torch.cuda.synchronize(dev)
         codes = ro.codes.cpu().numpy()
         scales = ro.scales.cpu().numpy()
         out[name] = {"codes_sha256": synth.sha256(codes), "scales_sha256": synth.sha256(scales),
                      "code_histogram": [int(v) for v in st["hist"]],
                      "sqnr_db": round(st["sqnr_db"], 4), "alpha": round(st["alpha"], 6),
-                     "shrinkage": round(st["shrinkage"], 6)}
+                     "shrinkage": round(st["shrinkage"], 6),
+                     "mean_rel_error": round(rel["mean"], 6),
+                     "grid_error_mean": round(ge["mean"], 6),
+                     "grid_error_per_level": [round(float(sm / c), 4) if c else None
+                                              for sm, c in zip(ge["sums"], ge["counts"])]}
     return out
 
 

@@ -16,7 +16,9 @@ fp32) are plain torch operations: they are the yardstick, not the path.
 * ``quantizer_report`` / ``delta_sqnr_sweep`` -- SQNR, attenuation, shrinkage
   and bucket ratio of one quantized copy after the inverse rotation, and the
   SQNR change that the rotation brings at rising outlier strength (same
-  section: E1M2 gains SQNR after the rotation, E2M1 often loses it).
+  section: E1M2 gains SQNR after the rotation, E2M1 often loses it), with the
+  per-element mean signed relative error and the rounding error in grid
+  units per level (Metodologia 1, "Origem Geometrica").
 * ``depth_chain`` -- K quantized GEMMs in a row, each layer's attenuation
   alpha_k against the exact product of its own input, their product, the
   first-order form exp(-sum delta_k) with delta_k = 1 - alpha_k, and the
@@ -62,8 +64,11 @@ def quantizer_report(x: torch.Tensor, grid: int, rot: int, sign_mask: int = 0, s
     deq = fp4q.dequantize(row, cfg, orient=0, unrotate=bool(rot), stream=stream)
     ref = x.float()
     s = fp4q.bias_stats(ref.reshape(-1), deq.reshape(-1), row.codes.reshape(-1), stream=stream)
+    rel = fp4q.rel_error(ref.reshape(-1), deq.reshape(-1), stream=stream)
+    ge = fp4q.grid_error(x, cfg, row, stream=stream)
     return {"sqnr_db": s["sqnr_db"], "alpha": s["alpha"], "shrinkage": s["shrinkage"],
-            "bucket_ratio": effective_bucket_ratio(s["hist"], grid), "hist": s["hist"], "sums": s["sums"]}
+            "bucket_ratio": effective_bucket_ratio(s["hist"], grid), "hist": s["hist"], "sums": s["sums"],
+            "mean_rel_error": rel["mean"], "grid_error": ge}
 
 
 def delta_sqnr_sweep(rows: int, cols: int, strengths, grids=(fp4q.GRID_E2M1, fp4q.GRID_E1M2, fp4q.GRID_E2M1_R4),

@@ -75,6 +75,12 @@ def lib() -> ctypes.CDLL:
         L.fp4q_workspace_bytes.argtypes = [i64, i64, P]
         L.fp4q_rht_quantize.restype = i32
         L.fp4q_rht_quantize.argtypes = [P, i64, i64, i64, P, P, P, P, sz, P, P]
+        L.fp4q_diag_workspace_bytes.restype = sz
+        L.fp4q_diag_workspace_bytes.argtypes = []
+        L.fp4q_grid_error.restype = i32
+        L.fp4q_grid_error.argtypes = [P, i64, i64, i64, P, P, P, sz, P, P]
+        L.fp4q_rel_error.restype = i32
+        L.fp4q_rel_error.argtypes = [P, P, i64, P, sz, P, P]
         L.fp4q_test_quantize_wait_expiry.restype = i32
         L.fp4q_test_quantize_wait_expiry.argtypes = [P, i64, i64, i64, P, P, P, P, sz, P, i32, u32, P]
         L.fp4q_rotated_amax.restype = i32
@@ -334,6 +340,32 @@ def bias_stats(ref: torch.Tensor, approx: torch.Tensor, codes: torch.Tensor | No
                               ctypes.byref(sh))
     return {"sums": sums, "n": int(ints[0]), "hist": ints[1:17], "sqnr_db": sq.value, "alpha": al.value,
             "shrinkage": sh.value}
+
+
+def grid_error(x: torch.Tensor, cfg: Config, row_copy: Operand, stream=None) -> dict:
+    """fp4q_grid_error: per level k, sum and count of g[k] - |v| (grid units)
+    over the row-wise copy of x; the overall mean."""
+    R, C = x.shape
+    ws = torch.empty(int(lib().fp4q_diag_workspace_bytes()), dtype=torch.uint8, device=x.device)
+    out = torch.empty(16, dtype=torch.float64, device=x.device)
+    cc, qc = cfg.c(), row_copy.c()
+    _check("fp4q_grid_error", lib().fp4q_grid_error(x.data_ptr(), R, C, x.stride(0), ctypes.byref(cc),
+                                                     ctypes.byref(qc), ws.data_ptr(), ws.numel(), out.data_ptr(),
+                                                     _stream(stream)))
+    h = out.cpu().numpy()
+    sums, counts = h[:8].copy(), h[8:].astype("uint64")
+    total = int(counts.sum())
+    return {"sums": sums, "counts": counts, "mean": float(sums.sum() / total) if total else float("nan")}
+
+
+def rel_error(ref: torch.Tensor, approx: torch.Tensor, stream=None) -> dict:
+    """fp4q_rel_error: mean of (|approx| - |ref|) / |ref| over ref != 0."""
+    ws = torch.empty(int(lib().fp4q_diag_workspace_bytes()), dtype=torch.uint8, device=ref.device)
+    out = torch.empty(2, dtype=torch.float64, device=ref.device)
+    _check("fp4q_rel_error", lib().fp4q_rel_error(ref.data_ptr(), approx.data_ptr(), ref.numel(), ws.data_ptr(),
+                                                   ws.numel(), out.data_ptr(), _stream(stream)))
+    s, c = out.cpu().tolist()
+    return {"sum": s, "count": int(c), "mean": s / c if c else float("nan")}
 
 
 def hadamard_rotate_bf16(x: torch.Tensor, rot: int, sign_mask_row: int = 0, sign_mask_col: int = 0,

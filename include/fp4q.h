@@ -275,6 +275,36 @@ void fp4q_bias_stats_noalloc_reset(void);
 /* Host helper: SQNR (dB), alpha and shrinkage from the five sums above. */
 void fp4q_stats_finalize(const double* sums5, double* sqnr_db, double* alpha, double* shrinkage);
 
+/* Diagnostics of the shrinkage bias ([SB] Metodologia 1, "Origem
+ * Geometrica"), deterministic fp64 reductions like fp4q_bias_stats.
+ *
+ * fp4q_grid_error: the rounding error in grid units of a ROW-WISE copy of the
+ * rows x cols bf16 x (row stride ld): per element, its position
+ * v = y * step^-1 on the grid (y the rotated value under cfg's rot and
+ * sign_mask_row, the step exactly as fp4q_rht_quantize takes it: 2^(127-sb)
+ * for MX, fl(1/fl(e4m3(sb) S_t)) for NV, 0 where an NV scale byte is 0) and
+ * its code's level g[k], k = code & 7.  out (device, 16 8-byte words): doubles
+ * sum over the elements of level k of g[k] - |v| for k = 0..7, then the counts
+ * of level k as doubles.  The mean of level k is the page's E[q - x | bin] =
+ * (l_i - r_i)/2 on locally uniform data.  cfg supplies grid, scale, rot,
+ * sign_mask_row and sf_layout (the copy's scale layout); a column-wise copy
+ * is the row-wise copy of the transposed input.
+ *
+ * fp4q_rel_error: sum over ref != 0 of (|approx| - |ref|) / |ref| and the
+ * number of such elements, two doubles in out (device): the per-element
+ * mean signed relative error is their quotient, reported beside the
+ * aggregate shrinkage of fp4q_bias_stats.
+ *
+ * Both take a device workspace of fp4q_diag_workspace_bytes() bytes
+ * (FP4Q_ERR_WORKSPACE if smaller) and are asynchronous on `stream`.
+ * Arguments: rows, cols > 0, cols % 32 == 0, ld >= cols with ld % 8 == 0,
+ * 16-byte aligned x, codes and workspace, 8-byte aligned out. */
+size_t fp4q_diag_workspace_bytes(void);
+int32_t fp4q_grid_error(const void* x, int64_t rows, int64_t cols, int64_t ld, const fp4q_config* cfg,
+                        const fp4q_operand* row_copy, void* workspace, size_t ws_bytes, void* out, void* stream);
+int32_t fp4q_rel_error(const float* ref, const float* approx, int64_t n, void* workspace, size_t ws_bytes,
+                       void* out, void* stream);
+
 /* Test of the quantizer's bounded waits (no page counterpart): the same call
  * as fp4q_rht_quantize, except that CTA 0 waits for its tile number
  * stall_tile (0 = its first tile) on a pipeline barrier that nothing arrives

@@ -27,6 +27,8 @@ def oracle_report(orc, bits, grid, rot, mask):
     deq = orc.dequantize(q["codes"], q["scales"], 0, grid, orc.SCALE_MX, True, rot, mask if rot else 0, bool(rot))
     st = orc.bias_stats(synth.bf16_bits_to_f32(bits).ravel(), deq.ravel(), q["codes"])
     st["bucket_ratio"] = orc.effective_bucket_ratio(st["hist"], grid)
+    st["mean_rel_error"] = orc.rel_error(synth.bf16_bits_to_f32(bits).ravel(), deq.ravel())["mean"]
+    st["grid_error"] = orc.grid_error(bits, grid, orc.SCALE_MX, rot, mask if rot else 0, q["codes"], q["scales"])
     return st
 
 
@@ -41,6 +43,9 @@ def test_quantizer_report_matches_oracle(dg, orc, grid, rot):
     assert np.allclose(got["sums"], want["sums"], rtol=1e-9, atol=0)
     assert got["bucket_ratio"] == pytest.approx(want["bucket_ratio"], rel=1e-12)
     assert got["sqnr_db"] == pytest.approx(want["sqnr_db"], rel=1e-9)
+    assert got["mean_rel_error"] == pytest.approx(want["mean_rel_error"], rel=1e-9)
+    assert np.array_equal(got["grid_error"]["counts"], want["grid_error"]["counts"])
+    assert got["grid_error"]["mean"] == pytest.approx(want["grid_error"]["mean"], abs=1e-6)
 
 
 def test_delta_sqnr_sweep(dg, orc):
