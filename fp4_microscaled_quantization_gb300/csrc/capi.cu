@@ -79,6 +79,8 @@ int32_t prepare(const void* x, int64_t rows, int64_t cols, int64_t ld, const fp4
   p.emit_e4m3 = cfg->emit_e4m3 ? 1 : 0;
   sign_words(cfg->sign_mask_row, cfg->rot, p.sgn_row);
   sign_words(cfg->sign_mask_col, cfg->rot, p.sgn_col);
+  for (int k = 0; k < 16; ++k) p.sw_row[k] = (p.sgn_row[2 * k] >> 16) | p.sgn_row[2 * k + 1];
+  for (int i = 0; i < 32; ++i) p.sw_col[i] = p.sgn_col[i] | (p.sgn_col[i] >> 16);
   p.stall_tile = -1;
   p.wait_limit_ns = 0;
   return FP4Q_OK;

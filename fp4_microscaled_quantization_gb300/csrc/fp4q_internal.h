@@ -29,6 +29,11 @@ struct QuantParams {
   int32_t want_row, want_col, sf_mma, emit_e4m3;
   uint32_t sgn_row[32];  // bit 31 set: negate element t of a 32-element chunk (row-wise)
   uint32_t sgn_col[32];  // same, column-wise copy
+  // The same signs for packed bf16 pairs (bit 15 negates the low element, bit
+  // 31 the high one): sw_row[k] for elements 2k, 2k+1 of a row-wise chunk;
+  // sw_col[i] for element i of both column chunks of a column pair.
+  uint32_t sw_row[16];
+  uint32_t sw_col[32];
   // Bounded-wait test (fp4q_test_quantize_wait_expiry only; 0 / -1 otherwise):
   // CTA 0 waits for its tile stall_tile on a barrier nothing arrives at, giving
   // up after wait_limit_ns instead of the usual ~2 s.

@@ -246,19 +246,91 @@ __device__ __forceinline__ void row_task(int t, int& r, int& q) {
 // ------------------------------------------------------------ fused kernel
 // Per tile each thread quantizes one column chunk (32 rows of one column, the
 // column-wise copy) and one row chunk (32 columns of one row, the row-wise
-// copy).
+// copy).  Signs are applied to the packed bf16 words with one XOR per word
+// (the sign words sw_row / sw_col of the kernel parameters) before the words
+// are widened to fp32.
+
+// Column c (0..255) of the tile's 32 rows as P[i] = (row i, row i + 16) with
+// the column copy's signs applied: one XOR per word (the sign word carries the
+// row's sign in both halves), then a byte permute with this thread's selector
+// brings its half of the word to the top and clears the rest.
+__device__ __forceinline__ void read_col_chunk_sw(const TileView& tv, int c, const uint32_t* sw, float2 (&P)[16]) {
+  const uint32_t sel = (c & 1) ? 0x3244u : 0x1044u;   // high half / low half to bits 16..31, zeros below
+  const uint8_t* b = tv.t + (c >> 6) * kBoxBytes + (((c >> 1) & 3) << 2);
+  const int x = (c >> 3) & 7;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint8_t* u = b + ((x ^ (i & 7)) << 4);   // rows i and i + 16 share the swizzle unit
+    const uint32_t a = *reinterpret_cast<const uint32_t*>(u + (i << 7)) ^ sw[i];
+    const uint32_t d = *reinterpret_cast<const uint32_t*>(u + ((i + 16) << 7)) ^ sw[i + 16];
+    P[i] = make_float2(__uint_as_float(__byte_perm(a, 0u, sel)), __uint_as_float(__byte_perm(d, 0u, sel)));
+  }
+}
+
+// Row-wise chunk q (0..7) of tile row r with the row copy's signs applied.
+__device__ __forceinline__ void read_row_chunk_sw(const TileView& tv, int r, int q, const uint32_t* sw,
+                                                  float2 (&P)[16]) {
+  const uint8_t* b = tv.t + (q >> 1) * kBoxBytes + (r << 7);
+  const int y = ((q & 1) << 2) ^ (r & 7);
+  uint32_t w[16];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint4 v = *reinterpret_cast<const uint4*>(b + ((y ^ j) << 4));
+    w[4 * j + 0] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
+  }
+  // word k holds elements 2k (low half) and 2k+1 (high half)
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t a = w[k] ^ sw[k], c = w[k + 8] ^ sw[k + 8];
+    P[2 * k] = make_float2(__uint_as_float(a << 16), __uint_as_float(c << 16));
+    P[2 * k + 1] = make_float2(__uint_as_float(a & 0xFFFF0000u), __uint_as_float(c & 0xFFFF0000u));
+  }
+}
+
 // Resident CTAs per SM: stochastic rounding runs Philox and the exact
 // round-up decision per element and does better with the register budget of
 // two CTAs per SM; the other modes with three.
 template <int ROUND>
 constexpr int quant_ctas() { return ROUND == FP4Q_SR ? 2 : QUANT_MIN_CTAS; }
 
+// Where one thread's chunks of a copy go: offsets that depend only on the
+// thread (fixed over the tiles) plus, per tile, the tile's own.
+struct ChunkDst {
+  int64_t code, scale, e4;   // byte offsets of the thread's first chunk in the current tile
+  int64_t code2, scale2, e42;   // the step to the thread's second chunk
+};
+
+// Scale, round, pack and store one chunk.
+template <int GRID, int SCALE, int NH, int ROUND>
+__device__ __forceinline__ void emit_chunk(float2 (&P)[16], const QuantParams& p, const CopyOut& d, float S_t,
+                                           uint64_t idx0, uint32_t orient, int64_t code_off, int64_t scale_off,
+                                           int64_t e4_off) {
+  constexpr bool kMX = SCALE == FP4Q_SCALE_MX;
+  ChunkOut o;
+  if constexpr (kMX) {
+    // H16's 1/4 goes into the power-of-two block scale
+    const float m = rotate_chunk_mx<NH>(P);
+    quantize_chunk<GRID, SCALE, ROUND, true>(P, S_t, idx0, orient, p.sr_keys, p.emit_e4m3, p.status, o,
+                                             NH == 16 ? 2 : 0, m);
+  } else {
+    rotate_chunk<NH>(P);
+    quantize_chunk<GRID, SCALE, ROUND>(P, S_t, idx0, orient, p.sr_keys, p.emit_e4m3, p.status, o);
+  }
+  *reinterpret_cast<uint4*>(d.codes + code_off) = make_uint4(o.w[0], o.w[1], o.w[2], o.w[3]);
+  if constexpr (kMX) d.scales[scale_off] = (uint8_t)o.sbytes;
+  else *reinterpret_cast<uint16_t*>(d.scales + scale_off) = (uint16_t)o.sbytes;
+  if (p.emit_e4m3) {
+    uint4* ep = reinterpret_cast<uint4*>(d.e4m3 + e4_off);
+    ep[0] = make_uint4(o.e4[0], o.e4[1], o.e4[2], o.e4[3]);
+    ep[1] = make_uint4(o.e4[4], o.e4[5], o.e4[6], o.e4[7]);
+  }
+}
+
 template <int GRID, int SCALE, int NH, int ROUND>
 __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
     rht_quant_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
   constexpr float kDen = 448.0f * GridK<GRID>::kQmax;
-  // MX with H16: the rotation's 1/4 goes into the power-of-two block scale
-  constexpr bool kFoldQuarter = SCALE == FP4Q_SCALE_MX && NH == 16;
+  constexpr int B = SCALE == FP4Q_SCALE_MX ? 32 : 16;
   float S_row = 0.0f, S_col = 0.0f;
   if constexpr (SCALE == FP4Q_SCALE_NV) {
     if (p.want_row) S_row = __fdiv_rn(p.gamax[0], kDen);
@@ -270,35 +342,56 @@ __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
   }
   TileRing ring;
   ring.init(&tmx, p.rows, p.cols, p.stall_tile, p.wait_limit_ns);
+
+  // ---- offsets of this thread's chunks that do not change from tile to tile
+  const int tid = threadIdx.x;
+  int rr, rq;
+  row_task(tid, rr, rq);
+  int64_t c_code = 0, c_scale = 0, c_e4 = 0, r_code = 0, r_scale = 0, r_e4 = 0;
+  if (p.want_col) {
+    const int64_t nkb = p.rows / B;
+    c_code = tid * (p.rows >> 1);
+    c_e4 = tid * p.rows;
+    c_scale = p.sf_mma ? (int64_t)(tid >> 7) * (nkb >> 2) * 512 + 16 * (tid & 31) + 4 * ((tid >> 5) & 3)
+                       : tid * nkb;
+  }
+  if (p.want_row) {
+    const int kq = rq * (32 / B);
+    r_code = rr * (p.cols >> 1) + 16 * rq;
+    r_e4 = rr * p.cols + 32 * rq;
+    r_scale = p.sf_mma ? (int64_t)((kq >> 2) * 512 + 16 * rr + (kq & 3)) : rr * (p.cols / B) + kq;
+  }
+
   int k = 0;
   for (int tile = blockIdx.x; tile < ring.ntiles; tile += gridDim.x, ++k) {
     if (!ring.wait(k, p.status)) return;
     const TileView tv = ring.view(k);
     const int64_t tr0 = (int64_t)(tile / ring.ntc) * kTR, tc0 = (int64_t)(tile % ring.ntc) * kTC;
     if (p.want_col) {
-      const int64_t c = tc0 + threadIdx.x;
-      if (c < p.cols && tr0 < p.rows) {
+      const int64_t c = tc0 + tid;
+      if (c < p.cols) {
+        // column c is row c of the column copy; the chunk covers its elements tr0 .. tr0 + 31
+        const int64_t nkb = p.rows / B, kb = tr0 / B;
+        const int64_t code = tc0 * (p.rows >> 1) + (tr0 >> 1) + c_code;
+        const int64_t e4 = tc0 * p.rows + tr0 + c_e4;
+        const int64_t scale =
+            (p.sf_mma ? (tc0 >> 7) * (nkb >> 2) * 512 + (kb >> 2) * 512 + (kb & 3) : tc0 * nkb + kb) + c_scale;
         float2 P[16];
-        read_col_chunk(tv, threadIdx.x, p.sgn_col, P);
-        rotate_chunk<NH, !kFoldQuarter>(P);
-        ChunkOut o;
-        quantize_chunk<GRID, SCALE, ROUND>(P, S_col, (uint64_t)(c * p.rows + tr0), 1u, p.sr_keys,
-                                           p.emit_e4m3, p.status, o, kFoldQuarter ? 2 : 0);
-        store_chunk<SCALE>(p.col, c, tr0, p.rows, p.sf_mma, p.emit_e4m3, o);
+        read_col_chunk_sw(tv, tid, p.sw_col, P);
+        emit_chunk<GRID, SCALE, NH, ROUND>(P, p, p.col, S_col, (uint64_t)(c * p.rows + tr0), 1u, code, scale, e4);
       }
     }
     if (p.want_row) {
-      int r, q;
-      row_task(threadIdx.x, r, q);
-      const int64_t gr = tr0 + r, gc = tc0 + 32 * q;
+      const int64_t gr = tr0 + rr, gc = tc0 + 32 * rq;
       if (gr < p.rows && gc < p.cols) {
+        const int64_t nkb = p.cols / B, kb = tc0 / B;
+        const int64_t code = tr0 * (p.cols >> 1) + (tc0 >> 1) + r_code;
+        const int64_t e4 = tr0 * p.cols + tc0 + r_e4;
+        const int64_t scale = (p.sf_mma ? ((tr0 >> 7) * (nkb >> 2) + (kb >> 2)) * 512 + 4 * ((tr0 >> 5) & 3)
+                                        : tr0 * nkb + kb) + r_scale;
         float2 P[16];
-        read_row_chunk(tv, r, q, p.sgn_row, P);
-        rotate_chunk<NH, !kFoldQuarter>(P);
-        ChunkOut o;
-        quantize_chunk<GRID, SCALE, ROUND>(P, S_row, (uint64_t)(gr * p.cols + gc), 0u, p.sr_keys,
-                                           p.emit_e4m3, p.status, o, kFoldQuarter ? 2 : 0);
-        store_chunk<SCALE>(p.row, gr, gc, p.cols, p.sf_mma, p.emit_e4m3, o);
+        read_row_chunk_sw(tv, rr, rq, p.sw_row, P);
+        emit_chunk<GRID, SCALE, NH, ROUND>(P, p, p.row, S_row, (uint64_t)(gr * p.cols + gc), 0u, code, scale, e4);
       }
     }
     ring.release(k, tile);

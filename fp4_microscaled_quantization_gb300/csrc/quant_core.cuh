@@ -160,6 +160,82 @@ __device__ __forceinline__ void rotate_chunk(float2 (&P)[16]) {
   }
 }
 
+// max(a, b, c) with NaN propagation (one three-input instruction).
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// Rotation of a chunk (signs applied) for an MX quantizer, returning the
+// block maximum max |P| of the result.  The maximum comes from the last
+// butterfly stage: of its two outputs fl(a + b) and fl(a - b) the larger
+// magnitude is fl(|a| + |b|) (round-to-nearest is monotone and odd, and
+// ||a| - |b|| <= |a| + |b|), so one add of magnitudes per output pair replaces
+// two maximum steps.  A NaN among a, b gives NaN either way; a +inf, -inf
+// pair gives inf where the outputs hold a NaN, and both lie above the finite
+// range, which is all an E8M0 scale reads of the maximum.  NH = 16 leaves out
+// the final 1/4 (the MX quantizer folds it into the block scale); NH = 32
+// applies c = fl(1/sqrt(32)) to every output and the maximum becomes fl(c M),
+// M the maximum before it (c > 0 keeps the order under rounding).
+template <int NH>
+__device__ __forceinline__ float rotate_chunk_mx(float2 (&P)[16]) {
+  if constexpr (NH == 16 || NH == 32) {
+    constexpr int kLastH = NH == 16 ? 8 : 16;   // the stride of the last packed stage left to the loop
+#pragma unroll
+    for (int h = 1; h < kLastH; h <<= 1) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (i & h) continue;
+        const float2 a = P[i], b = P[i + h];
+        P[i] = add2(a, b);
+        P[i + h] = sub2(a, b);
+      }
+    }
+    float s[16];
+    if constexpr (NH == 16) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float2 a = P[i], b = P[i + 8];
+        s[2 * i] = __fadd_rn(fabsf(a.x), fabsf(b.x));
+        s[2 * i + 1] = __fadd_rn(fabsf(a.y), fabsf(b.y));
+        P[i] = add2(a, b);
+        P[i + 8] = sub2(a, b);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float a = P[i].x, b = P[i].y;
+        s[i] = __fadd_rn(fabsf(a), fabsf(b));
+        P[i].x = __fadd_rn(a, b);
+        P[i].y = __fsub_rn(a, b);
+      }
+    }
+    float m = max_nan(max3_nan(max3_nan(s[0], s[1], s[2]), max3_nan(s[3], s[4], s[5]), max3_nan(s[6], s[7], s[8])),
+                      max3_nan(max3_nan(s[9], s[10], s[11]), max3_nan(s[12], s[13], s[14]), s[15]));
+    if constexpr (NH == 32) {
+      const float c = __uint_as_float(0x3E3504F3u);   // fl32(1/sqrt(32))
+#pragma unroll
+      for (int i = 0; i < 16; ++i) P[i] = mul2(P[i], make_float2(c, c));
+      m = __fmul_rn(m, c);
+    }
+    return m;
+  } else {
+    float m0 = 0.0f, m1 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      m0 = absmax_nan(m0, P[i].x);
+      m1 = absmax_nan(m1, P[i].y);
+    }
+    return fabsf(absmax_nan(m0, m1));
+  }
+}
+
 // A chunk of 32 bf16 values given as 16 words (word k holds elements 2k in
 // its low half and 2k+1 in its high half), widened to fp32 pairs
 // P[i] = (u[i], u[i+16]) with the sign words applied.  For a low half,
@@ -192,23 +268,29 @@ struct ChunkOut {
 //          subnormal blocks, pre being taken off before the clamp), and
 //          v = P 2^(127 - pre - sb) is the same real number as y 2^(127 - sb)
 //          with the same single rounding.
-template <int GRID, int SCALE, int ROUND>
+//   GIVEN  MX only: m_given is the block maximum max |P| (rotate_chunk_mx)
+//          instead of a maximum taken here.
+template <int GRID, int SCALE, int ROUND, bool GIVEN = false>
 __device__ __forceinline__ void quantize_chunk(float2 (&P)[16], float S_t, uint64_t idx0,
                                                uint32_t orient, const uint32_t (&rk)[20],
-                                               bool emit_e4m3, uint32_t* status, ChunkOut& o, int pre = 0) {
+                                               bool emit_e4m3, uint32_t* status, ChunkOut& o, int pre = 0,
+                                               float m_given = 0.0f) {
   constexpr float QMAX = GridK<GRID>::kQmax;
-  // block amax (NaN-propagating)
+  static_assert(!GIVEN || SCALE == FP4Q_SCALE_MX, "a given maximum is an MX block maximum");
+  // block amax (NaN-propagating) of each 16-lane half
   float m0 = 0.0f, m1 = 0.0f;
+  if constexpr (!GIVEN) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    m0 = absmax_nan(m0, P[i].x);
-    m1 = absmax_nan(m1, P[i].y);
+    for (int i = 0; i < 16; ++i) {
+      m0 = absmax_nan(m0, P[i].x);
+      m1 = absmax_nan(m1, P[i].y);
+    }
+    m0 = fabsf(m0);
+    m1 = fabsf(m1);
   }
-  m0 = fabsf(m0);
-  m1 = fabsf(m1);
   float2 vm;
   if constexpr (SCALE == FP4Q_SCALE_MX) {
-    const float m = fabsf(absmax_nan(m0, m1));
+    const float m = GIVEN ? m_given : fabsf(absmax_nan(m0, m1));
     const uint32_t mb = __float_as_uint(m);
     if (mb >= 0x7F800000u) raise_status(status, FP4Q_DEV_NONFINITE);
     int sb = (int)(mb >> 23) - GridK<GRID>::kEmax - pre;   // floor(log2 m) - e_max + 127, 0 for m = 0
