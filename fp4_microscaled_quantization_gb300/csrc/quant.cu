@@ -362,11 +362,20 @@ __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
     r_scale = p.sf_mma ? (int64_t)((kq >> 2) * 512 + 16 * rr + (kq & 3)) : rr * (p.cols / B) + kq;
   }
 
+  // the tile's (row, column) position, stepped by the grid size without a division per tile
+  int t_r = blockIdx.x / ring.ntc, t_c = blockIdx.x % ring.ntc;
+  const int d_r = gridDim.x / ring.ntc, d_c = gridDim.x % ring.ntc;
   int k = 0;
   for (int tile = blockIdx.x; tile < ring.ntiles; tile += gridDim.x, ++k) {
     if (!ring.wait(k, p.status)) return;
     const TileView tv = ring.view(k);
-    const int64_t tr0 = (int64_t)(tile / ring.ntc) * kTR, tc0 = (int64_t)(tile % ring.ntc) * kTC;
+    const int64_t tr0 = (int64_t)t_r * kTR, tc0 = (int64_t)t_c * kTC;
+    t_c += d_c;
+    t_r += d_r;
+    if (t_c >= ring.ntc) {
+      t_c -= ring.ntc;
+      ++t_r;
+    }
     if (p.want_col) {
       const int64_t c = tc0 + tid;
       if (c < p.cols) {
