@@ -37,10 +37,11 @@
 //   epilogue    (warps 2-5 and 10-13; 2-5 when the kernel quantizes its
 //               output) TMEM -> registers (tcgen05.ld), alpha, fp32 / bf16,
 //               the accumulator is released to the next tile's MMAs, then
-//               the stores: straight from registers to global memory in the
-//               plain kernels; through a swizzled shared-memory slice (TMA
-//               store, then the row-wise quantization of the slice) in the
-//               kernels that quantize their output.
+//               the stores by TMA: through 32-row x 32-byte boxes staged in
+//               1 KB per warp in the plain kernels; through a 128-byte
+//               swizzled 32 x 256 slice per warp in the kernels that quantize
+//               their output (TMA store, then the row-wise quantization of the
+//               slice).
 // Signals between the two CTAs are relaxed cluster-scope mbarrier arrivals:
 // what they announce is already complete when they are sent (TMEM writes
 // waited for with tcgen05.wait::st, TMEM reads with tcgen05.wait::ld), and a
