@@ -90,27 +90,41 @@ constexpr int KROW = 128;            // bytes of one operand row per K-tile (one
 constexpr int A_BYTES = BM * KROW;   // 16 KB: this CTA's rows of A
 constexpr int B_BYTES = 128 * KROW;  // 16 KB: this CTA's half of B
 constexpr int OP_STAGE = A_BYTES + B_BYTES;
+static_assert(A_BYTES == B_BYTES, "one descriptor step per K-span for both operands");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;      // accumulator columns [0, 256); scale slots after it
 constexpr int kSmemMax = 232448;     // dynamic shared memory per CTA
 constexpr int kBarBytes = 512;       // barriers, TMEM address, abort flag
 
+#ifndef FP4Q_GEMM_KT
+#define FP4Q_GEMM_KT 2
+#endif
+
 template <int KIND, bool FUSED = false>
 struct KindK {
+  // K-spans per stage: a span is one 128-byte (128B-swizzle) piece of every
+  // operand row.  Two spans (eight MMAs per stage barrier) halve the stage
+  // boundaries, where the tensor pipe idles; NVF4's scale columns and the
+  // fused kernels' shared-memory staging leave room for one only.
+  static constexpr int kKT = (KIND == KIND_NVF4 || FUSED) ? 1 : FP4Q_GEMM_KT;
   // chunks = 512-byte groups of 4 consecutive scale bytes of one 128-row group
-  static constexpr int kChunks = KIND == KIND_MXF4 ? 2 : (KIND == KIND_NVF4 ? 4 : 1);   // per K-tile
-  static constexpr int kElemsPerTile = KIND == KIND_F8 ? 128 : 256;
+  static constexpr int kChunks = kKT * (KIND == KIND_MXF4 ? 2 : (KIND == KIND_NVF4 ? 4 : 1));   // per stage
+  static constexpr int kElemsPerTile = kKT * (KIND == KIND_F8 ? 128 : 256);                     // K per stage
   static constexpr int kMmaK = KIND == KIND_F8 ? 32 : 64;
+  static constexpr int kMmas = kElemsPerTile / kMmaK;                                          // per stage
   static constexpr int kBlock = KIND == KIND_NVF4 ? 16 : 32;
+  // a stage's operands: kKT spans of A (A_BYTES each), then kKT spans of B
+  static constexpr int kOpStage = kKT * OP_STAGE;
   // one stage's compact chunks: A (kChunks), B row group 0 (kChunks), B row
   // group 1 (kChunks), loaded with the stage's operands into its slot
   static constexpr int kSfBytes = 3 * kChunks * 512;
-  static constexpr int kSlot = OP_STAGE + (kSfBytes + 1023) / 1024 * 1024;
-  // TMEM scale columns of a stage: A 4 per chunk, B 8 per chunk; a slot is
-  // written with one x32 store (MXF4), x32 + x16 (NVF4) or one x16 (F8)
+  static constexpr int kSlot = kOpStage + (kSfBytes + 1023) / 1024 * 1024;
+  // TMEM scale columns of a stage: A 4 per chunk, B 8 per chunk, rounded up
+  // to the stores that write them (x16, x32 or x32 + x16)
   static constexpr int kSfColsA = 4 * kChunks;
   static constexpr int kSfColsB = 8 * kChunks;
-  static constexpr int kSfCols = KIND == KIND_MXF4 ? 32 : (KIND == KIND_NVF4 ? 48 : 16);
+  static constexpr int kSfCols = (kSfColsA + kSfColsB + 15) / 16 * 16;
+  static_assert(kSfCols == 16 || kSfCols == 32 || kSfCols == 48, "scale slot stores");
   // every stage has its TMEM scale slot beside the accumulator
   static constexpr int kStagesTmem = (int)(TMEM_COLS - 256) / kSfCols;
   // threads: producer, MMA, scale-writer warps, the epilogue warps (8, two
@@ -518,10 +532,14 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
           }
           const uint32_t st = sbase + (uint32_t)s * SLOT;
           const uint32_t fb = lead_full + 8 * s;
-          cluster_expect_tx(fb, OP_STAGE);
-          // rows past M or N (a 128-row tail) are zero-filled and still counted
-          tma_load_2d_pair(st, mA, kt * KROW, t.m0, fb);
-          tma_load_2d_pair(st + A_BYTES, mB, kt * KROW, t.n0 + 128 * (int)rank, fb);
+          cluster_expect_tx(fb, KK::kOpStage);
+          // rows past M or N (a 128-row tail) and spans past K are zero-filled and still counted
+#pragma unroll
+          for (int j = 0; j < KK::kKT; ++j) {
+            const int x = (kt * KK::kKT + j) * KROW;
+            tma_load_2d_pair(st + j * A_BYTES, mA, x, t.m0, fb);
+            tma_load_2d_pair(st + KK::kKT * A_BYTES + j * B_BYTES, mB, x, t.n0 + 128 * (int)rank, fb);
+          }
         }
       }
       // The leader's commits arrive on this CTA's empty barriers: wait for the
@@ -556,11 +574,14 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
           const uint32_t sfa_col = tmem + ACC_COL + BN + SF_COLS * s;
           const uint32_t sfb_col = sfa_col + KK::kSfColsA;
           const int rem = t.K - kt * KK::kElemsPerTile;
-          const int n_mma = min(4, rem / KK::kMmaK);
-          // descriptors of K slice k: the start address field advances by 32 bytes (2 units of 16)
-          const uint64_t da = op_desc(st), db = op_desc(st + A_BYTES);
+          const int n_mma = min(KK::kMmas, rem / KK::kMmaK);
+          // MMA k reads span k / 4 (its own 128-byte swizzle span of every
+          // row); inside the span the descriptors' start address advances by
+          // 32 bytes (2 units of 16) per MMA
+          const uint64_t da = op_desc(st), db = op_desc(st + KK::kKT * A_BYTES);
           const uint32_t acc0 = kt > 0 ? 1u : 0u;
           auto issue = [&](int k) {
+            // the 4-byte scale chunk of MMA k and the scale bytes inside it
             uint32_t sfa = sfa_col, sfb = sfb_col, sf_id = 0;
             if constexpr (KIND == KIND_MXF4) {
               sfa += 4 * (k >> 1);
@@ -570,16 +591,17 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
               sfa += 4 * k;
               sfb += 8 * k;
             } else {
-              sf_id = (uint32_t)k;
+              sfa += 4 * (k >> 2);
+              sfb += 8 * (k >> 2);
+              sf_id = (uint32_t)(k & 3);
             }
             const uint32_t acc = k > 0 ? 1u : acc0;
-            tc_mma_pair<KIND>(tmem + ACC_COL, da + 2u * k, db + 2u * k, make_idesc<KIND>(sf_id), sfa, sfb, acc);
+            const uint64_t off = (uint64_t)((A_BYTES >> 4) * (k >> 2) + 2 * (k & 3));   // A_BYTES == B_BYTES
+            tc_mma_pair<KIND>(tmem + ACC_COL, da + off, db + off, make_idesc<KIND>(sf_id), sfa, sfb, acc);
           };
-          if (n_mma == 4) {
-            issue(0);
-            issue(1);
-            issue(2);
-            issue(3);
+          if (n_mma == KK::kMmas) {
+#pragma unroll
+            for (int k = 0; k < KK::kMmas; ++k) issue(k);
           } else {
             for (int k = 0; k < n_mma; ++k) issue(k);
           }
@@ -629,7 +651,7 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
           }
           const int q0 = kt * KK::kChunks;
           const uint32_t sf_bytes = (uint32_t)min(KK::kChunks, t.nq - q0) * 512u;
-          const uint32_t sb = bar_sfd + 8 * s, ca = sbase + (uint32_t)s * SLOT + OP_STAGE;
+          const uint32_t sb = bar_sfd + 8 * s, ca = sbase + (uint32_t)s * SLOT + KK::kOpStage;
           mbar_expect_tx(sb, sf_bytes * ((rows ? 1u : 0u) + (rg1 ? 2u : 1u)));
           if (rows) bulk_load(ca, sfa_t + (size_t)q0 * 512, sf_bytes, sb);
           bulk_load(ca + KK::kChunks * 512, sfb_t + (size_t)q0 * 512, sf_bytes, sb);
@@ -659,7 +681,7 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t ca = sbase + s * SLOT + OP_STAGE, cb0 = ca + KK::kChunks * 512, cb1 = cb0 + KK::kChunks * 512;
+        const uint32_t ca = sbase + s * SLOT + KK::kOpStage, cb0 = ca + KK::kChunks * 512, cb1 = cb0 + KK::kChunks * 512;
         const uint32_t sfa_col = qbase + ACC_COL + BN + SF_COLS * s;
         // the slot's columns in order: A chunks (4 each), then per B chunk its two row groups
         uint32_t wv[KK::kSfCols];
