@@ -272,6 +272,26 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 // This warp's TMEM lane quarter, 32 (16) consecutive 32-bit columns from taddr.
+// 64 consecutive fp32 accumulator columns of this thread's TMEM lane, one
+// load and one wait.  `dep` (the packed bf16 words of the previous 64
+// columns, unused by the instruction) orders the load after their conversion,
+// so that no more than one load's registers are live at a time.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64], const uint32_t* dep) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr), "r"(dep[0]), "r"(dep[1]), "r"(dep[2]), "r"(dep[3]), "r"(dep[4]), "r"(dep[5]), "r"(dep[6]), "r"(dep[7]), "r"(dep[8]), "r"(dep[9]), "r"(dep[10]), "r"(dep[11]), "r"(dep[12]), "r"(dep[13]), "r"(dep[14]), "r"(dep[15]), "r"(dep[16]), "r"(dep[17]), "r"(dep[18]), "r"(dep[19]), "r"(dep[20]), "r"(dep[21]), "r"(dep[22]), "r"(dep[23]), "r"(dep[24]), "r"(dep[25]), "r"(dep[26]), "r"(dep[27]), "r"(dep[28]), "r"(dep[29]), "r"(dep[30]), "r"(dep[31]));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* w) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -830,19 +850,23 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
         // accumulator is released.
         constexpr int ECOLS = KK::kEpiCols, UNITS = (int)BOXB / 16;   // 16-byte units per box row
         constexpr int FCOLS = (int)BOXB / 4, HCOLS = (int)BOXB / 2;   // columns of an fp32 / bf16 box
+        constexpr int LCOLS = 64;                                     // columns per TMEM load
+        static_assert(ECOLS % LCOLS == 0 && ECOLS / 2 >= 32, "epilogue columns");
         uint32_t h[ECOLS / 2];   // this warp's columns of the row as packed bf16
 #pragma unroll
-        for (int c0 = 0; c0 < ECOLS; c0 += 32) {
-          if (cbase + c0 < ncols) {
-            uint32_t r[32];
-            tmem_ld32(lane_base + (uint32_t)(cbase + c0), r);
+        for (int j = 0; j < ECOLS / 2; ++j) h[j] = 0u;
+#pragma unroll
+        for (int c0 = 0; c0 < ECOLS; c0 += LCOLS) {
+          if (cbase + c0 < ncols) {   // ncols is 128 or 256: a load never straddles the edge
+            uint32_t r[LCOLS];
+            tmem_ld64(lane_base + (uint32_t)(cbase + c0), r, h + (c0 > 0 ? c0 / 2 - 32 : 0));
             if constexpr (KIND == KIND_NVF4) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), alpha));
+              for (int j = 0; j < LCOLS; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), alpha));
             }
             if (want_f32 && live) {
 #pragma unroll
-              for (int hh = 0; hh < 32 / FCOLS; ++hh) {
+              for (int hh = 0; hh < LCOLS / FCOLS; ++hh) {
                 if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
                 __syncwarp();
 #pragma unroll
@@ -859,7 +883,7 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
               }
             }
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < LCOLS / 2; ++j) {
               const __nv_bfloat162 b2 =
                   __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
               h[c0 / 2 + j] = *reinterpret_cast<const uint32_t*>(&b2);
