@@ -59,9 +59,6 @@ __device__ __forceinline__ uint32_t rtne_e1m2(float v) {
   return (__float_as_uint(t) & 7u) | ((__float_as_uint(v) >> 28) & 8u);
 }
 
-// 2^23 + r as a float, r the 16-bit uniform numerator (exact).
-__device__ __forceinline__ float r16_float(uint32_t r16) { return __uint_as_float(0x4B000000u | r16); }
-
 // Stochastic rounding, two elements at a time: the fp32 steps are packed
 // f32x2 instructions, each lane rounded as the scalar instruction would be.
 __device__ __forceinline__ uint64_t pack2(float2 a) {
@@ -76,11 +73,13 @@ __device__ __forceinline__ float2 unpack2(uint64_t d) {
 }
 // Exact decision shared by all grids.  With s >= 0 the position on a
 // unit-spaced grid (s < 8), t = fl_rm(s + 2^23) holds floor(s) in its low
-// bits; C = 2^39 + 2^23 - t 2^16 = 2^23 - floor(s) 2^16 is exact; y =
-// fl_ru(s 2^16 + C) = 2^23 + ceil(frac(s) 2^16); and r16 < frac(s) 2^16 (the
-// rule r / 2^16 < f) holds iff 2^23 + r16 < y.  Returns floor(s) + up; rf is
-// r16_float of the element's random numerator.
-__device__ __forceinline__ uint2 sr_unit2(float2 s, float2 rf) {
+// bits (bits(t) = 0x4B000000 + floor(s)); C = 2^39 + 2^23 - t 2^16 =
+// 2^23 - floor(s) 2^16 is exact; y = fl_ru(s 2^16 + C) = 2^23 +
+// ceil(frac(s) 2^16), so bits(y) - 0x4B000000 is that integer; and the rule
+// r / 2^16 < frac(s) holds iff r < ceil(frac(s) 2^16), i.e. iff the 32-bit
+// difference r + 0x4B000000 - bits(y) is negative.  Returns bits(t) and
+// that difference's sign bit per lane.
+__device__ __forceinline__ uint4 sr_unit2(float2 s, uint32_t rx, uint32_t ry) {
   uint64_t t, c, y;
   const uint64_t ss = pack2(s);
   asm("add.rm.f32x2 %0, %1, %2;" : "=l"(t) : "l"(ss), "l"(pack2(make_float2(8388608.0f, 8388608.0f))));
@@ -90,29 +89,38 @@ __device__ __forceinline__ uint2 sr_unit2(float2 s, float2 rf) {
         "l"(pack2(make_float2(549764202496.0f, 549764202496.0f))));
   asm("fma.rp.f32x2 %0, %1, %2, %3;" : "=l"(y) : "l"(ss), "l"(pack2(make_float2(65536.0f, 65536.0f))), "l"(c));
   const float2 tt = unpack2(t), yy = unpack2(y);
-  return make_uint2((__float_as_uint(tt.x) & 7u) + ((rf.x < yy.x) ? 1u : 0u),
-                    (__float_as_uint(tt.y) & 7u) + ((rf.y < yy.y) ? 1u : 0u));
+  return make_uint4(__float_as_uint(tt.x), (rx + 0x4B000000u - __float_as_uint(yy.x)) >> 31,
+                    __float_as_uint(tt.y), (ry + 0x4B000000u - __float_as_uint(yy.y)) >> 31);
 }
-// SR onto {k/4}: s = 4 min(|v|, 1.75) is exact and lies on the unit grid.
-__device__ __forceinline__ uint2 sr_e1m2_2(float2 v, float2 rf) {
+// The SR codes below come out offset by a constant (kSrOff), which spares a
+// mask or correction per element; a packed word of eight codes is corrected
+// once by kSrOff * 0x11111111 (the eight nibbles are added modulo 2^32).
+template <int GRID>
+struct SrOff {
+  static constexpr uint32_t kSrOff = GRID == FP4Q_GRID_E1M2 ? 0x4B000000u : 0x4B0000FEu;
+};
+// SR onto {k/4}: s = 4 min(|v|, 1.75) is exact and lies on the unit grid;
+// code + kSrOff = bits(t) + up + 8 sign.
+__device__ __forceinline__ uint2 sr_e1m2_2(float2 v, uint32_t rx, uint32_t ry) {
   const float2 s = mul2(make_float2(fminf(fabsf(v.x), 1.75f), fminf(fabsf(v.y), 1.75f)), make_float2(4.0f, 4.0f));
-  const uint2 u = sr_unit2(s, rf);
-  return make_uint2(u.x | ((__float_as_uint(v.x) >> 28) & 8u), u.y | ((__float_as_uint(v.y) >> 28) & 8u));
+  const uint4 u = sr_unit2(s, rx, ry);
+  return make_uint2(u.x + u.y + ((__float_as_uint(v.x) >> 31) << 3), u.z + u.w + ((__float_as_uint(v.y) >> 31) << 3));
 }
 // SR onto E2M1: with E = clamp(floor(log2 |v|), 0, 2) the levels around |v|
 // are 2^(E-1) apart, s = |v| 2^(1-E) is exact (2^(1-E) has exponent field
 // 0x7F800000 - eb, eb = (127 + E) << 23), and the lower level's code is
-// 2E + floor(s) (floor(s) = 0..3 for E = 0, 2..3 above).
+// 2E + floor(s) (floor(s) = 0..3 for E = 0, 2..3 above); eb >> 22 = 254 + 2E,
+// so code + kSrOff = bits(t) + (eb >> 22) + up + 8 sign.
 template <int CAP = 6>
-__device__ __forceinline__ uint2 sr_e2m1_2(float2 v, float2 rf) {
+__device__ __forceinline__ uint2 sr_e2m1_2(float2 v, uint32_t rx, uint32_t ry) {
   const float ax = fminf(fabsf(v.x), (float)CAP), ay = fminf(fabsf(v.y), (float)CAP);
   const uint32_t ebx = __float_as_uint(fmaxf(ax, 1.0f)) & 0x7F800000u;
   const uint32_t eby = __float_as_uint(fmaxf(ay, 1.0f)) & 0x7F800000u;
   const float2 s = mul2(make_float2(ax, ay),
                         make_float2(__uint_as_float(0x7F800000u - ebx), __uint_as_float(0x7F800000u - eby)));
-  const uint2 u = sr_unit2(s, rf);
-  return make_uint2((((ebx >> 22) - 254u) + u.x) | ((__float_as_uint(v.x) >> 28) & 8u),
-                    (((eby >> 22) - 254u) + u.y) | ((__float_as_uint(v.y) >> 28) & 8u));
+  const uint4 u = sr_unit2(s, rx, ry);
+  return make_uint2(u.x + (ebx >> 22) + u.y + ((__float_as_uint(v.x) >> 31) << 3),
+                    u.z + (eby >> 22) + u.w + ((__float_as_uint(v.y) >> 31) << 3));
 }
 
 // E4M3 bytes of eight packed codes (element 0 in the low nibble): magnitude by
@@ -357,19 +365,20 @@ __device__ __forceinline__ void quantize_chunk(float2 (&P)[16], float S_t, uint6
       const uint64_t ca = c + (uint64_t)h, cb = ca + 2u;
       const Philox4 ra = philox4x32_10_rk((uint32_t)ca, (uint32_t)(ca >> 32), orient, 0u, rk);
       const Philox4 rb = philox4x32_10_rk((uint32_t)cb, (uint32_t)(cb >> 32), orient, 0u, rk);
+      constexpr uint32_t kSrPack = SrOff<GRID>::kSrOff * 0x11111111u;
       uint32_t wa = 0, wb = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float2 rf = (j & 1) ? make_float2(r16_float(ra.v[j >> 1] >> 16), r16_float(rb.v[j >> 1] >> 16))
-                                  : make_float2(r16_float(ra.v[j >> 1] & 0xFFFFu), r16_float(rb.v[j >> 1] & 0xFFFFu));
-        const uint2 code = (GRID == FP4Q_GRID_E1M2) ? sr_e1m2_2(P[8 * h + j], rf)
-                           : (GRID == FP4Q_GRID_E2M1_R4) ? sr_e2m1_2<4>(P[8 * h + j], rf)
-                                                         : sr_e2m1_2<6>(P[8 * h + j], rf);
-        wa |= code.x << (4 * j);
-        wb |= code.y << (4 * j);
+        const uint32_t rx = (j & 1) ? (ra.v[j >> 1] >> 16) : (ra.v[j >> 1] & 0xFFFFu);
+        const uint32_t ry = (j & 1) ? (rb.v[j >> 1] >> 16) : (rb.v[j >> 1] & 0xFFFFu);
+        const uint2 code = (GRID == FP4Q_GRID_E1M2) ? sr_e1m2_2(P[8 * h + j], rx, ry)
+                           : (GRID == FP4Q_GRID_E2M1_R4) ? sr_e2m1_2<4>(P[8 * h + j], rx, ry)
+                                                         : sr_e2m1_2<6>(P[8 * h + j], rx, ry);
+        wa += code.x << (4 * j);
+        wb += code.y << (4 * j);
       }
-      o.w[h] = wa;
-      o.w[h + 2] = wb;
+      o.w[h] = wa - kSrPack;
+      o.w[h + 2] = wb - kSrPack;
     }
   }
   if (emit_e4m3) {
