@@ -122,8 +122,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 
 // Persistent walk over the tiles of the matrix: CTA b takes tiles b, b + G,
 // b + 2G, ... (G = gridDim.x, column tiles fastest).  Thread 0 keeps kStages
-// TMA tile loads in flight; all threads wait on the tile's mbarrier, compute,
-// and meet at a barrier before the stage is refilled.  Used inline in each
+// TMA tile loads in flight; every thread waits on the tile's mbarrier itself,
+// computes, and all meet at one barrier per tile before the stage is refilled.  Used inline in each
 // kernel so that the kernel parameters stay constant-bank operands.
 struct TileRing {
   uint8_t* smem;
@@ -171,12 +171,21 @@ struct TileRing {
     }
   }
 
-  // Wait for the k-th tile of this CTA; false (after raising FP4Q_DEV_TIMEOUT
-  // and draining this CTA's own loads) when it did not arrive in time.
-  __device__ __forceinline__ bool wait(int k, uint32_t* status) const {
+  __device__ __forceinline__ TileView view(int k) const { return TileView{smem + (k % kStages) * kTileBytes}; }
+
+  // This thread's bounded wait for the k-th tile of this CTA (no CTA
+  // barrier: every thread waits on the tile's mbarrier itself).
+  __device__ __forceinline__ bool wait(int k) const {
     const int s = k % kStages;
-    const bool ok = k == stall_tile ? mbar_wait_bounded(bar0 + 8 * kStages, 0u, stall_limit_ns)
-                                    : mbar_wait_bounded(bar0 + 8 * s, (uint32_t)(k / kStages) & 1u);
+    return k == stall_tile ? mbar_wait_bounded(bar0 + 8 * kStages, 0u, stall_limit_ns)
+                           : mbar_wait_bounded(bar0 + 8 * s, (uint32_t)(k / kStages) & 1u);
+  }
+
+  // All threads are done with the k-th tile (ok: this thread saw it arrive):
+  // the one CTA barrier of a tile, then thread 0 refills its stage.  Returns
+  // false, after raising FP4Q_DEV_TIMEOUT and draining this CTA's own loads,
+  // when any thread's wait ran out; every thread then leaves together.
+  __device__ __forceinline__ bool release(int k, int tile, bool ok, uint32_t* status) const {
     if (__syncthreads_or(!ok)) {
       if (threadIdx.x == 0) {
         raise_status(status, FP4Q_DEV_TIMEOUT);
@@ -188,18 +197,11 @@ struct TileRing {
       __syncthreads();
       return false;
     }
-    return true;
-  }
-
-  __device__ __forceinline__ TileView view(int k) const { return TileView{smem + (k % kStages) * kTileBytes}; }
-
-  // All threads are done with the k-th tile: refill its stage.
-  __device__ __forceinline__ void release(int k, int tile) const {
-    __syncthreads();
     if (threadIdx.x == 0) {
       const int nt = tile + kStages * gridDim.x;
       if (nt < ntiles) issue(k % kStages, nt);
     }
+    return true;
   }
 };
 
@@ -367,7 +369,7 @@ __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
   const int d_r = gridDim.x / ring.ntc, d_c = gridDim.x % ring.ntc;
   int k = 0;
   for (int tile = blockIdx.x; tile < ring.ntiles; tile += gridDim.x, ++k) {
-    if (!ring.wait(k, p.status)) return;
+    const bool arrived = ring.wait(k);
     const TileView tv = ring.view(k);
     const int64_t tr0 = (int64_t)t_r * kTR, tc0 = (int64_t)t_c * kTC;
     t_c += d_c;
@@ -376,7 +378,7 @@ __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
       t_c -= ring.ntc;
       ++t_r;
     }
-    if (p.want_col) {
+    if (arrived && p.want_col) {
       const int64_t c = tc0 + tid;
       if (c < p.cols) {
         // column c is row c of the column copy; the chunk covers its elements tr0 .. tr0 + 31
@@ -390,7 +392,7 @@ __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
         emit_chunk<GRID, SCALE, NH, ROUND>(P, p, p.col, S_col, (uint64_t)(c * p.rows + tr0), 1u, code, scale, e4);
       }
     }
-    if (p.want_row) {
+    if (arrived && p.want_row) {
       const int64_t gr = tr0 + rr, gc = tc0 + 32 * rq;
       if (gr < p.rows && gc < p.cols) {
         const int64_t nkb = p.cols / B, kb = tc0 / B;
@@ -403,7 +405,7 @@ __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
         emit_chunk<GRID, SCALE, NH, ROUND>(P, p, p.row, S_row, (uint64_t)(gr * p.cols + gc), 0u, code, scale, e4);
       }
     }
-    ring.release(k, tile);
+    if (!ring.release(k, tile, arrived, p.status)) return;
   }
 }
 
@@ -421,17 +423,17 @@ __global__ void __launch_bounds__(kNT, QUANT_MIN_CTAS) rotated_amax_kernel(const
   ring.init(&tmx, p.rows, p.cols);
   int k = 0;
   for (int tile = blockIdx.x; tile < ring.ntiles; tile += gridDim.x, ++k) {
-    if (!ring.wait(k, p.status)) return;
+    const bool arrived = ring.wait(k);
     const TileView tv = ring.view(k);
     // zero-filled padding contributes |0| and cannot raise the maximum
-    if (p.want_col) {
+    if (arrived && p.want_col) {
       float2 P[16];
       read_col_chunk(tv, threadIdx.x, p.sgn_col, P);
       rotate_chunk<NH>(P);
 #pragma unroll
       for (int i = 0; i < 16; ++i) mcol = absmax_nan(mcol, absmax_nan(P[i].x, P[i].y));
     }
-    if (p.want_row) {
+    if (arrived && p.want_row) {
       int r, q;
       row_task(threadIdx.x, r, q);
       float2 P[16];
@@ -440,7 +442,7 @@ __global__ void __launch_bounds__(kNT, QUANT_MIN_CTAS) rotated_amax_kernel(const
 #pragma unroll
       for (int i = 0; i < 16; ++i) mrow = absmax_nan(mrow, absmax_nan(P[i].x, P[i].y));
     }
-    ring.release(k, tile);
+    if (!ring.release(k, tile, arrived, p.status)) return;
   }
   mrow = fabsf(mrow);
   mcol = fabsf(mcol);
@@ -542,10 +544,10 @@ __global__ void __launch_bounds__(kNT, QUANT_MIN_CTAS) rotate_bf16_kernel(const 
   ring.init(&tmx, p.rows, p.cols);
   int k = 0;
   for (int tile = blockIdx.x; tile < ring.ntiles; tile += gridDim.x, ++k) {
-    if (!ring.wait(k, p.status)) return;
+    const bool arrived = ring.wait(k);
     const TileView tv = ring.view(k);
     const int64_t tr0 = (int64_t)(tile / ring.ntc) * kTR, tc0 = (int64_t)(tile % ring.ntc) * kTC;
-    if (y_col) {
+    if (arrived && y_col) {
       const int64_t c = tc0 + threadIdx.x;
       if (c < p.cols && tr0 < p.rows) {
         float2 P[16];
@@ -558,7 +560,7 @@ __global__ void __launch_bounds__(kNT, QUANT_MIN_CTAS) rotate_bf16_kernel(const 
         }
       }
     }
-    if (y_row) {
+    if (arrived && y_row) {
       int r, q;
       row_task(threadIdx.x, r, q);
       const int64_t gr = tr0 + r, gc = tc0 + 32 * q;
@@ -577,7 +579,7 @@ __global__ void __launch_bounds__(kNT, QUANT_MIN_CTAS) rotate_bf16_kernel(const 
         for (int j = 0; j < 4; ++j) dst[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
       }
     }
-    ring.release(k, tile);
+    if (!ring.release(k, tile, arrived, p.status)) return;
   }
 }
 
