@@ -97,7 +97,7 @@ __device__ __forceinline__ uint4 sr_unit2(float2 s, uint32_t rx, uint32_t ry) {
 // once by kSrOff * 0x11111111 (the eight nibbles are added modulo 2^32).
 template <int GRID>
 struct SrOff {
-  static constexpr uint32_t kSrOff = GRID == FP4Q_GRID_E1M2 ? 0x4B000000u : 0x4B0000FEu;
+  static constexpr uint32_t kSrOff = GRID == FP4Q_GRID_E1M2 ? 0x4B000000u : 0x4AFFFF00u;
 };
 // SR onto {k/4}: s = 4 min(|v|, 1.75) is exact and lies on the unit grid;
 // code + kSrOff = bits(t) + up + 8 sign.
@@ -107,20 +107,22 @@ __device__ __forceinline__ uint2 sr_e1m2_2(float2 v, uint32_t rx, uint32_t ry) {
   return make_uint2(u.x + u.y + ((__float_as_uint(v.x) >> 31) << 3), u.z + u.w + ((__float_as_uint(v.y) >> 31) << 3));
 }
 // SR onto E2M1: with E = clamp(floor(log2 |v|), 0, 2) the levels around |v|
-// are 2^(E-1) apart, s = |v| 2^(1-E) is exact (2^(1-E) has exponent field
-// 0x7F800000 - eb, eb = (127 + E) << 23), and the lower level's code is
-// 2E + floor(s) (floor(s) = 0..3 for E = 0, 2..3 above); eb >> 22 = 254 + 2E,
-// so code + kSrOff = bits(t) + (eb >> 22) + up + 8 sign.
+// are 2^(E-1) apart, s = |v| 2^(1-E) is exact, and the lower level's code is
+// 2E + floor(s) (floor(s) = 0..3 for E = 0, 2..3 above).  With e = 127 + E
+// the exponent field of max(|v|, 1), m = ~bits & 0x7F800000 = (255 - e) << 23
+// is the bit pattern of 2^(1-E), and m >> 22 = 256 - 2E, so
+// code + kSrOff = bits(t) - (m >> 22) + up + 8 sign.
 template <int CAP = 6>
 __device__ __forceinline__ uint2 sr_e2m1_2(float2 v, uint32_t rx, uint32_t ry) {
   const float ax = fminf(fabsf(v.x), (float)CAP), ay = fminf(fabsf(v.y), (float)CAP);
-  const uint32_t ebx = __float_as_uint(fmaxf(ax, 1.0f)) & 0x7F800000u;
-  const uint32_t eby = __float_as_uint(fmaxf(ay, 1.0f)) & 0x7F800000u;
-  const float2 s = mul2(make_float2(ax, ay),
-                        make_float2(__uint_as_float(0x7F800000u - ebx), __uint_as_float(0x7F800000u - eby)));
+  // ~bits & exponent mask = (255 - e) << 23, the bits of 2^(1-E) (e = 127 + E)
+  const uint32_t mx = ~__float_as_uint(fmaxf(ax, 1.0f)) & 0x7F800000u;
+  const uint32_t my = ~__float_as_uint(fmaxf(ay, 1.0f)) & 0x7F800000u;
+  const float2 s = mul2(make_float2(ax, ay), make_float2(__uint_as_float(mx), __uint_as_float(my)));
   const uint4 u = sr_unit2(s, rx, ry);
-  return make_uint2(u.x + (ebx >> 22) + u.y + ((__float_as_uint(v.x) >> 31) << 3),
-                    u.z + (eby >> 22) + u.w + ((__float_as_uint(v.y) >> 31) << 3));
+  // m >> 22 = 510 - 2e = 256 - 2E
+  return make_uint2(u.x - (mx >> 22) + u.y + ((__float_as_uint(v.x) >> 31) << 3),
+                    u.z - (my >> 22) + u.w + ((__float_as_uint(v.y) >> 31) << 3));
 }
 
 // E4M3 bytes of eight packed codes (element 0 in the low nibble): magnitude by
