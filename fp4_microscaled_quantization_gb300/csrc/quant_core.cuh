@@ -51,12 +51,11 @@ __device__ __forceinline__ uint32_t cap_e2m1_codes(uint32_t w) {
 }
 
 // ------------------------------------------------------------ rounding
-// RTNE onto {k/4}: clamp |v| to 1.75, then k = RNE(4|v|) read from the low
-// mantissa bits of 4|v| + 2^23 (exact product, one rounding).
-__device__ __forceinline__ uint32_t rtne_e1m2(float v) {
-  const float a = fminf(fabsf(v), 1.75f);
-  const float t = __fmaf_rn(a, 4.0f, 8388608.0f);
-  return (__float_as_uint(t) & 7u) | ((__float_as_uint(v) >> 28) & 8u);
+// RTNE onto {k/4}: clamp |v| to 1.75, then t = fl(4|v| + 2^23) (exact
+// product, one round-to-nearest-even) holds k = RNE(4|v|) in its low bits;
+// returns bits(t) = 0x4B000000 + k.
+__device__ __forceinline__ uint32_t rtne_e1m2_bits(float v) {
+  return __float_as_uint(__fmaf_rn(fminf(fabsf(v), 1.75f), 4.0f, 8388608.0f));
 }
 
 // Stochastic rounding, two elements at a time: the fp32 steps are packed
@@ -344,6 +343,9 @@ __device__ __forceinline__ void quantize_chunk(float2 (&P)[16], float S_t, uint6
       for (int q = 0; q < 4; ++q) o.w[q] = cap_e2m1_codes(o.w[q]);
     }
   } else if constexpr (ROUND == FP4Q_RTNE) {
+    // E1M2: each code is carried as bits(t) + 8 sign = code + 0x4B000000 and
+    // the packed word corrected once
+    constexpr uint32_t kPack = 0x4B000000u * 0x11111111u;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       uint32_t w = 0;
@@ -351,9 +353,9 @@ __device__ __forceinline__ void quantize_chunk(float2 (&P)[16], float S_t, uint6
       for (int j = 0; j < 8; ++j) {
         const int i = (q & 1) * 8 + j;
         const float v = (q < 2) ? P[i].x : P[i].y;
-        w |= rtne_e1m2(v) << (4 * j);
+        w += (rtne_e1m2_bits(v) + ((__float_as_uint(v) >> 31) << 3)) << (4 * j);
       }
-      o.w[q] = w;
+      o.w[q] = w - kPack;
     }
   } else {
     // stochastic rounding: element t of the chunk takes half (t & 1) of word
