@@ -39,13 +39,16 @@ bool encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, ui
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The current device's SM count, cached per device; 0 when it cannot be
+// queried, which makes every persistent grid empty and its launch fail with
+// an error status instead of running on a guessed size.
 int num_sms() {
   static int cache[64] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
   if (dev < 64 && cache[dev]) return cache[dev];
   int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
   if (dev < 64) cache[dev] = n;
   return n;
 }
