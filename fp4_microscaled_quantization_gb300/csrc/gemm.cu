@@ -14,14 +14,17 @@
 // 128r..128r+127 of each tile in its TMEM, loads those rows of A and rows
 // 128r..128r+127 of B, and the pair's MMAs, issued by rank 0 (the leader),
 // read both CTAs' shared memory.  Each SM so pulls 32 KB of operands per
-// K-tile of 256 out of L2 for 128 x 256 x 256 of MMA work, which L2 sustains;
-// a lone CTA on the same tile width would need 48 KB.  Roles (per CTA):
+// 128-byte K-span (256 FP4 elements of every row) out of L2 for 128 x 256 x
+// 256 of MMA work, which L2 sustains; a lone CTA on the same tile width would
+// need 48 KB.  A stage holds two K-spans (kKT) for kind::mxf4 and
+// mxf8f6f4: eight MMAs per stage barrier, because every stage boundary is a
+// pipe bubble.  Roles (per CTA):
 //   warp 0      producer: A rows and this CTA's half of B by
 //               cp.async.bulk.tensor (.cta_group::2, 128-byte swizzled
-//               K-major rows) into a ring of kStages slots, the bytes
-//               completing on the leader's full barrier of the slot (two TMA
-//               instructions per stage: issuing them is not free, so the
-//               scale chunks have a loader of their own).
+//               K-major rows, one box per operand and K-span) into a ring of
+//               kStages slots, the bytes completing on the leader's full
+//               barrier of the slot (issuing TMA instructions is not free, so
+//               the scale chunks have a loader of their own).
 //   warp 1      owns the TMEM allocation (cta_group::2); on the leader one
 //               lane waits for a stage (one barrier: both CTAs' operands and
 //               both CTAs' scale writers), issues its MMAs back to back and
@@ -35,8 +38,10 @@
 //               stage's TMEM scale slot with tcgen05.st and arrives on the
 //               stage's barrier in the leader.
 //   epilogue    (warps 2-5 and 10-13; 2-5 when the kernel quantizes its
-//               output) TMEM -> registers (tcgen05.ld), alpha, fp32 / bf16,
-//               the accumulator is released to the next tile's MMAs, then
+//               output) TMEM -> registers (tcgen05.ld, 64 columns a load in
+//               the plain kernels), alpha, fp32 / bf16, the accumulator is
+//               released to the next tile's MMAs (the one accumulator is
+//               single-buffered: the next tile's MMAs wait for it), then
 //               the stores by TMA: through 32-row x 32-byte boxes staged in
 //               1 KB per warp in the plain kernels; through a 128-byte
 //               swizzled 32 x 256 slice per warp in the kernels that quantize
