@@ -13,11 +13,14 @@
 //         E8M0 shared exponent, nearest 4-bit value).
 //
 // Design (GB300-first, HBM-bound):
-//   * Persistent CTAs (three per SM) walk 32 x 256 bf16 tiles (16 KB).  Each
-//     tile is read once from HBM by TMA into a 4-stage shared-memory ring
-//     (128-byte swizzle), so three tiles are in flight while one is computed.
-//     Both the row-wise copy (blocks along columns) and the column-wise copy
-//     (blocks along rows, stored transposed) come from that one read.
+//   * Persistent CTAs (three per SM for RTNE, two for stochastic rounding)
+//     walk 32 x 256 bf16 tiles (16 KB).  Each tile is read once from HBM by
+//     TMA into a shared-memory ring (128-byte swizzle) of two tiles (RTNE) or
+//     three (SR): the depths measured fastest.  Every thread waits on the
+//     tile's mbarrier itself and the CTA meets once per tile, before the
+//     stage is refilled.  Both the row-wise copy (blocks along columns) and
+//     the column-wise copy (blocks along rows, stored transposed) come from
+//     that one read.
 //   * A "chunk" is 32 consecutive elements of one row or one column.  A thread
 //     holds a chunk as 16 fp32 pairs P[i] = (u[i], u[i+16]) so that every
 //     butterfly stage of stride < 16 is one packed FADD2/FFMA2 over two
