@@ -31,6 +31,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -712,7 +714,34 @@ def cpu_baseline(args, rows: int = 1024, min_s: float = 10.0) -> dict:
     return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "cpu_model": cpu_model(),
             "host_threads": os.cpu_count(), "kind": "oracle",
             "sample": f"quantize (both copies) of rows 0..{rows - 1} of X and dY and rows 0..{Ws.shape[0] - 1} "
-                      f"of W of the same workload, {n} repetitions, {dt:.2f} s each; GEMMs not included"}
+                      f"of W of the same workload, {n} repetitions, {dt:.2f} s each; the GEMMs in `gemm`",
+            "gemm": cpu_gemm_sample(orc, Xs, Ws, mK)}
+
+
+def cpu_gemm_sample(orc, Xs, Ws, mK, entries: int = 65536, min_s: float = 3.0) -> dict:
+    """The oracle's GEMM (one fp64 dot per output entry, single-threaded C) on
+    sampled Fprop outputs of the same workload: the rows of X and W that the
+    quantize sample holds, quantized and dequantized by the oracle, and
+    `entries` seeded (row, column) pairs with K = 4096."""
+    qa = orc.quantize(Xs, 0, 0, orc.SCALE_MX, 16, mK)
+    qb = orc.quantize(Ws, 0, 0, orc.SCALE_MX, 16, mK)
+    A = orc.dequantize(qa["codes"], qa["scales"], 0.0, 0, orc.SCALE_MX)
+    B = orc.dequantize(qb["codes"], qb["scales"], 0.0, 0, orc.SCALE_MX)
+    g = np.random.Generator(np.random.PCG64(SEED))
+    ii = g.integers(0, A.shape[0], entries)
+    jj = g.integers(0, B.shape[0], entries)
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        orc.gemm_entries(A, B, ii, jj)
+        n += 1
+        if time.perf_counter() - t0 >= min_s:
+            break
+    dt = (time.perf_counter() - t0) / n
+    flops = 2.0 * entries * A.shape[1]
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
+            "sample": f"{entries} sampled Fprop outputs (K = {A.shape[1]}) of the oracle-quantized rows 0..{A.shape[0] - 1} "
+                      f"of X and 0..{B.shape[0] - 1} of W, {n} repetitions, {dt:.2f} s each"}
 
 
 def run_reference(args, world, rank):
