@@ -261,7 +261,9 @@ __device__ __forceinline__ void row_task(int t, int& r, int& q) {
 // Column c (0..255) of the tile's 32 rows as P[i] = (row i, row i + 16) with
 // the column copy's signs applied: one XOR per word (the sign word carries the
 // row's sign in both halves), then a byte permute with this thread's selector
-// brings its half of the word to the top and clears the rest.
+// brings its half of the word to the top and clears the rest.  SIGNS = false
+// (no rotation, all sign words zero) leaves the XORs out.
+template <bool SIGNS>
 __device__ __forceinline__ void read_col_chunk_sw(const TileView& tv, int c, const uint32_t* sw, float2 (&P)[16]) {
   const uint32_t sel = (c & 1) ? 0x3244u : 0x1044u;   // high half / low half to bits 16..31, zeros below
   const uint8_t* b = tv.t + (c >> 6) * kBoxBytes + (((c >> 1) & 3) << 2);
@@ -269,13 +271,15 @@ __device__ __forceinline__ void read_col_chunk_sw(const TileView& tv, int c, con
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const uint8_t* u = b + ((x ^ (i & 7)) << 4);   // rows i and i + 16 share the swizzle unit
-    const uint32_t a = *reinterpret_cast<const uint32_t*>(u + (i << 7)) ^ sw[i];
-    const uint32_t d = *reinterpret_cast<const uint32_t*>(u + ((i + 16) << 7)) ^ sw[i + 16];
+    const uint32_t a = *reinterpret_cast<const uint32_t*>(u + (i << 7)) ^ (SIGNS ? sw[i] : 0u);
+    const uint32_t d = *reinterpret_cast<const uint32_t*>(u + ((i + 16) << 7)) ^ (SIGNS ? sw[i + 16] : 0u);
     P[i] = make_float2(__uint_as_float(__byte_perm(a, 0u, sel)), __uint_as_float(__byte_perm(d, 0u, sel)));
   }
 }
 
-// Row-wise chunk q (0..7) of tile row r with the row copy's signs applied.
+// Row-wise chunk q (0..7) of tile row r with the row copy's signs applied
+// (none for SIGNS = false).
+template <bool SIGNS>
 __device__ __forceinline__ void read_row_chunk_sw(const TileView& tv, int r, int q, const uint32_t* sw,
                                                   float2 (&P)[16]) {
   const uint8_t* b = tv.t + (q >> 1) * kBoxBytes + (r << 7);
@@ -289,7 +293,7 @@ __device__ __forceinline__ void read_row_chunk_sw(const TileView& tv, int r, int
   // word k holds elements 2k (low half) and 2k+1 (high half)
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const uint32_t a = w[k] ^ sw[k], c = w[k + 8] ^ sw[k + 8];
+    const uint32_t a = w[k] ^ (SIGNS ? sw[k] : 0u), c = w[k + 8] ^ (SIGNS ? sw[k + 8] : 0u);
     P[2 * k] = make_float2(__uint_as_float(a << 16), __uint_as_float(c << 16));
     P[2 * k + 1] = make_float2(__uint_as_float(a & 0xFFFF0000u), __uint_as_float(c & 0xFFFF0000u));
   }
@@ -399,7 +403,7 @@ __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
         const int64_t scale =
             (p.sf_mma ? (tc0 >> 7) * (nkb >> 2) * 512 + (kb >> 2) * 512 + (kb & 3) : tc0 * nkb + kb) + c_scale;
         float2 P[16];
-        read_col_chunk_sw(tv, tid, p.sw_col, P);
+        read_col_chunk_sw<(NH > 0)>(tv, tid, p.sw_col, P);
         emit_chunk<GRID, SCALE, NH, ROUND>(P, p, p.col, S_col, (uint64_t)(c * p.rows + tr0), 1u, code, scale, e4);
       }
     }
@@ -412,7 +416,7 @@ __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
         const int64_t scale = (p.sf_mma ? ((tr0 >> 7) * (nkb >> 2) + (kb >> 2)) * 512 + 4 * ((tr0 >> 5) & 3)
                                         : tr0 * nkb + kb) + r_scale;
         float2 P[16];
-        read_row_chunk_sw(tv, rr, rq, p.sw_row, P);
+        read_row_chunk_sw<(NH > 0)>(tv, rr, rq, p.sw_row, P);
         emit_chunk<GRID, SCALE, NH, ROUND>(P, p, p.row, S_row, (uint64_t)(gr * p.cols + gc), 0u, code, scale, e4);
       }
     }
