@@ -51,13 +51,6 @@ __device__ __forceinline__ uint32_t cap_e2m1_codes(uint32_t w) {
 }
 
 // ------------------------------------------------------------ rounding
-// RTNE onto {k/4}: clamp |v| to 1.75, then t = fl(4|v| + 2^23) (exact
-// product, one round-to-nearest-even) holds k = RNE(4|v|) in its low bits;
-// returns bits(t) = 0x4B000000 + k.
-__device__ __forceinline__ uint32_t rtne_e1m2_bits(float v) {
-  return __float_as_uint(__fmaf_rn(fminf(fabsf(v), 1.75f), 4.0f, 8388608.0f));
-}
-
 // Stochastic rounding, two elements at a time: the fp32 steps are packed
 // f32x2 instructions, each lane rounded as the scalar instruction would be.
 __device__ __forceinline__ uint64_t pack2(float2 a) {
@@ -70,58 +63,62 @@ __device__ __forceinline__ float2 unpack2(uint64_t d) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
   return r;
 }
-// Exact decision shared by all grids.  With s >= 0 the position on a
-// unit-spaced grid (s < 8), t = fl_rm(s + 2^23) holds floor(s) in its low
-// bits (bits(t) = 0x4B000000 + floor(s)); C = 2^39 + 2^23 - t 2^16 =
-// 2^23 - floor(s) 2^16 is exact; y = fl_ru(s 2^16 + C) = 2^23 +
-// ceil(frac(s) 2^16), so bits(y) - 0x4B000000 is that integer; and the rule
-// r / 2^16 < frac(s) holds iff r < ceil(frac(s) 2^16), i.e. iff the 32-bit
-// difference r + 0x4B000000 - bits(y) is negative.  Returns bits(t) and
-// that difference's sign bit per lane.
-__device__ __forceinline__ uint4 sr_unit2(float2 s, uint32_t rx, uint32_t ry) {
-  uint64_t t, c, y;
-  const uint64_t ss = pack2(s);
-  asm("add.rm.f32x2 %0, %1, %2;" : "=l"(t) : "l"(ss), "l"(pack2(make_float2(8388608.0f, 8388608.0f))));
-  asm("fma.rn.f32x2 %0, %1, %2, %3;"
-      : "=l"(c)
-      : "l"(t), "l"(pack2(make_float2(-65536.0f, -65536.0f))),
-        "l"(pack2(make_float2(549764202496.0f, 549764202496.0f))));
-  asm("fma.rp.f32x2 %0, %1, %2, %3;" : "=l"(y) : "l"(ss), "l"(pack2(make_float2(65536.0f, 65536.0f))), "l"(c));
-  const float2 tt = unpack2(t), yy = unpack2(y);
-  return make_uint4(__float_as_uint(tt.x), (rx + 0x4B000000u - __float_as_uint(yy.x)) >> 31,
-                    __float_as_uint(tt.y), (ry + 0x4B000000u - __float_as_uint(yy.y)) >> 31);
+// Exact decision shared by all grids.  The magnitude codes are the integers
+// 0..7 and each grid is linear between neighbouring codes, so SR acts on the
+// position p (0 <= p < 8) of |v| in code units: with u = r / 2^16 the draw,
+// the rounded code is floor(p) + [u < frac(p)] = ceil(p - u) = n.  The
+// argument is a = p / 2^L (the product a 2^(16 + L) is exact).  The operand
+// -(2^23 + r) is exact (bits 0xCB000000 | r, passed as nx, ny); the exact
+// x = p 2^16 - 2^23 - r is at most n 2^16 - 2^23, which is representable, so
+// d = fl_ru(x) lies in [x, n 2^16 - 2^23], d 2^-16 + 128 lies in [p - u, n],
+// and y = fl_ru(d 2^-16 + 2^23 + 129), on the unit-spaced binade [2^23, 2^24),
+// is 2^23 + 1 + n exactly: bits(y) = 0x4B000001 + n per lane.
+// The result is unchanged when p is replaced by any p' between p and the
+// next multiple of 2^-16 at or above it (n + u is such a multiple, so
+// p - u <= p' - u <= n), e.g. p rounded upward in fp32.
+constexpr uint32_t kSrOff = 0x4B000001u;
+template <int L>
+__device__ __forceinline__ uint2 sr_code2(float2 a, uint32_t nx, uint32_t ny) {
+  constexpr float kMul = 65536.0f * (float)(1 << L);
+  uint64_t d, y;
+  asm("fma.rp.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(pack2(a)), "l"(pack2(make_float2(kMul, kMul))),
+        "l"(pack2(make_float2(__uint_as_float(nx), __uint_as_float(ny)))));
+  asm("fma.rp.f32x2 %0, %1, %2, %3;"
+      : "=l"(y)
+      : "l"(d), "l"(pack2(make_float2(1.0f / 65536.0f, 1.0f / 65536.0f))),
+        "l"(pack2(make_float2(8388737.0f, 8388737.0f))));
+  const float2 yy = unpack2(y);
+  return make_uint2(__float_as_uint(yy.x), __float_as_uint(yy.y));
 }
-// The SR codes below come out offset by a constant (kSrOff), which spares a
-// mask or correction per element; a packed word of eight codes is corrected
-// once by kSrOff * 0x11111111 (the eight nibbles are added modulo 2^32).
-template <int GRID>
-struct SrOff {
-  static constexpr uint32_t kSrOff = GRID == FP4Q_GRID_E1M2 ? 0x4B000000u : 0x4AFFFF00u;
-};
-// SR onto {k/4}: s = 4 min(|v|, 1.75) is exact and lies on the unit grid;
-// code + kSrOff = bits(t) + up + 8 sign.
-__device__ __forceinline__ uint2 sr_e1m2_2(float2 v, uint32_t rx, uint32_t ry) {
-  const float2 s = mul2(make_float2(fminf(fabsf(v.x), 1.75f), fminf(fabsf(v.y), 1.75f)), make_float2(4.0f, 4.0f));
-  const uint4 u = sr_unit2(s, rx, ry);
-  return make_uint2(u.x + u.y + ((__float_as_uint(v.x) >> 31) << 3), u.z + u.w + ((__float_as_uint(v.y) >> 31) << 3));
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
-// SR onto E2M1: with E = clamp(floor(log2 |v|), 0, 2) the levels around |v|
-// are 2^(E-1) apart, s = |v| 2^(1-E) is exact, and the lower level's code is
-// 2E + floor(s) (floor(s) = 0..3 for E = 0, 2..3 above).  With e = 127 + E
-// the exponent field of max(|v|, 1), m = ~bits & 0x7F800000 = (255 - e) << 23
-// is the bit pattern of 2^(1-E), and m >> 22 = 256 - 2E, so
-// code + kSrOff = bits(t) - (m >> 22) + up + 8 sign.
+// The codes come out offset by kSrOff, which spares a correction per element;
+// a packed word of eight codes is corrected once by kSrOff * 0x11111111 (the
+// eight nibbles are added modulo 2^32).  Signs are merged into the word
+// separately.  fminf drops a NaN, so a NaN magnitude takes the top code.
+// SR onto {k/4}: p = 4 min(|v|, 1.75).
+__device__ __forceinline__ uint2 sr_e1m2_2(float2 v, uint32_t nx, uint32_t ny) {
+  return sr_code2<2>(make_float2(fminf(fabsf(v.x), 1.75f), fminf(fabsf(v.y), 1.75f)), nx, ny);
+}
+// SR onto E2M1 (levels 0, 0.5, 1, 1.5, 2, 3, 4, 6; CAP 4 for the capped
+// grid): the position is concave and piecewise linear in a = min(|v|, CAP),
+// slope 2 up to 2, 1 up to 4, 1/2 up to 6, so p = a + min(a, 2, 4 - a/2).
+// The inner minimum is exact wherever it matters: 4 - a/2 is exact for
+// a >= 4 (Sterbenz), and below 4 it exceeds 2, which its rounding keeps.
+// p itself is rounded upward.
 template <int CAP = 6>
-__device__ __forceinline__ uint2 sr_e2m1_2(float2 v, uint32_t rx, uint32_t ry) {
-  const float ax = fminf(fabsf(v.x), (float)CAP), ay = fminf(fabsf(v.y), (float)CAP);
-  // ~bits & exponent mask = (255 - e) << 23, the bits of 2^(1-E) (e = 127 + E)
-  const uint32_t mx = ~__float_as_uint(fmaxf(ax, 1.0f)) & 0x7F800000u;
-  const uint32_t my = ~__float_as_uint(fmaxf(ay, 1.0f)) & 0x7F800000u;
-  const float2 s = mul2(make_float2(ax, ay), make_float2(__uint_as_float(mx), __uint_as_float(my)));
-  const uint4 u = sr_unit2(s, rx, ry);
-  // m >> 22 = 510 - 2e = 256 - 2E
-  return make_uint2(u.x - (mx >> 22) + u.y + ((__float_as_uint(v.x) >> 31) << 3),
-                    u.z - (my >> 22) + u.w + ((__float_as_uint(v.y) >> 31) << 3));
+__device__ __forceinline__ uint2 sr_e2m1_2(float2 v, uint32_t nx, uint32_t ny) {
+  const float2 a = make_float2(fminf(fabsf(v.x), (float)CAP), fminf(fabsf(v.y), (float)CAP));
+  const float2 t = __ffma2_rn(a, make_float2(-0.5f, -0.5f), make_float2(4.0f, 4.0f));
+  const float2 m = make_float2(min3f(a.x, 2.0f, t.x), min3f(a.y, 2.0f, t.y));
+  uint64_t p;
+  asm("add.rp.f32x2 %0, %1, %2;" : "=l"(p) : "l"(pack2(a)), "l"(pack2(m)));
+  return sr_code2<0>(unpack2(p), nx, ny);
 }
 
 // E4M3 bytes of eight packed codes (element 0 in the low nibble): magnitude by
@@ -343,19 +340,44 @@ __device__ __forceinline__ void quantize_chunk(float2 (&P)[16], float S_t, uint6
       for (int q = 0; q < 4; ++q) o.w[q] = cap_e2m1_codes(o.w[q]);
     }
   } else if constexpr (ROUND == FP4Q_RTNE) {
-    // E1M2: each code is carried as bits(t) + 8 sign = code + 0x4B000000 and
-    // the packed word corrected once
+    // E1M2: t = fl(4 min(|v|, 1.75) + 2^23) (exact product, one
+    // round-to-nearest-even) holds the code in its low bits, bits(t) =
+    // 0x4B000000 + code; the code words are corrected once.  With NV scales
+    // elements 8h + j (P[8h + j].x, word h) and 16 + 8h + j (its .y, word
+    // h + 2) are rounded as one packed pair and the signs merged as in the SR
+    // branch below (132.7 against 138.9 us for X 16384x4096); with MX scales
+    // the scalar form measured faster (99.0 against 103.0 us with E4M3 bytes).
     constexpr uint32_t kPack = 0x4B000000u * 0x11111111u;
+    if constexpr (SCALE == FP4Q_SCALE_NV) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t w = 0;
+      for (int h = 0; h < 2; ++h) {
+        uint32_t wa = 0, wb = 0, sa = 0, sb = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int i = (q & 1) * 8 + j;
-        const float v = (q < 2) ? P[i].x : P[i].y;
-        w += (rtne_e1m2_bits(v) + ((__float_as_uint(v) >> 31) << 3)) << (4 * j);
+        for (int j = 7; j >= 0; --j) {
+          const float2 v = P[8 * h + j];
+          const float2 t = __ffma2_rn(make_float2(fminf(fabsf(v.x), 1.75f), fminf(fabsf(v.y), 1.75f)),
+                                      make_float2(4.0f, 4.0f), make_float2(8388608.0f, 8388608.0f));
+          wa += __float_as_uint(t.x) << (4 * j);
+          wb += __float_as_uint(t.y) << (4 * j);
+          sa = __funnelshift_l(__float_as_uint(v.x), sa, 4);
+          sb = __funnelshift_l(__float_as_uint(v.y), sb, 4);
+        }
+        o.w[h] = (wa - kPack) | (sa & 0x88888888u);
+        o.w[h + 2] = (wb - kPack) | (sb & 0x88888888u);
       }
-      o.w[q] = w - kPack;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t w = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = (q & 1) * 8 + j;
+          const float v = (q < 2) ? P[i].x : P[i].y;
+          const uint32_t t = __float_as_uint(__fmaf_rn(fminf(fabsf(v), 1.75f), 4.0f, 8388608.0f));
+          w += (t + ((__float_as_uint(v) >> 31) << 3)) << (4 * j);
+        }
+        o.w[q] = w - kPack;
+      }
     }
   } else {
     // stochastic rounding: element t of the chunk takes half (t & 1) of word
@@ -369,20 +391,27 @@ __device__ __forceinline__ void quantize_chunk(float2 (&P)[16], float S_t, uint6
       const uint64_t ca = c + (uint64_t)h, cb = ca + 2u;
       const Philox4 ra = philox4x32_10_rk((uint32_t)ca, (uint32_t)(ca >> 32), orient, 0u, rk);
       const Philox4 rb = philox4x32_10_rk((uint32_t)cb, (uint32_t)(cb >> 32), orient, 0u, rk);
-      constexpr uint32_t kSrPack = SrOff<GRID>::kSrOff * 0x11111111u;
-      uint32_t wa = 0, wb = 0;
+      constexpr uint32_t kSrPack = kSrOff * 0x11111111u;
+      uint32_t wa = 0, wb = 0, sa = 0, sb = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t rx = (j & 1) ? (ra.v[j >> 1] >> 16) : (ra.v[j >> 1] & 0xFFFFu);
-        const uint32_t ry = (j & 1) ? (rb.v[j >> 1] >> 16) : (rb.v[j >> 1] & 0xFFFFu);
-        const uint2 code = (GRID == FP4Q_GRID_E1M2) ? sr_e1m2_2(P[8 * h + j], rx, ry)
-                           : (GRID == FP4Q_GRID_E2M1_R4) ? sr_e2m1_2<4>(P[8 * h + j], rx, ry)
-                                                         : sr_e2m1_2<6>(P[8 * h + j], rx, ry);
+      for (int j = 7; j >= 0; --j) {
+        // bits of -(2^23 + r): the 16-bit half of the Philox word under 0xCB00
+        const uint32_t sel = (j & 1) ? 0x7632u : 0x7610u;
+        const uint32_t nx = __byte_perm(ra.v[j >> 1], 0xCB000000u, sel);
+        const uint32_t ny = __byte_perm(rb.v[j >> 1], 0xCB000000u, sel);
+        const float2 v = P[8 * h + j];
+        const uint2 code = (GRID == FP4Q_GRID_E1M2) ? sr_e1m2_2(v, nx, ny)
+                           : (GRID == FP4Q_GRID_E2M1_R4) ? sr_e2m1_2<4>(v, nx, ny)
+                                                         : sr_e2m1_2<6>(v, nx, ny);
         wa += code.x << (4 * j);
         wb += code.y << (4 * j);
+        // signs: the earlier elements move up one nibble and the top four bits
+        // of v (its sign in bit 3) enter nibble 0; element j ends in nibble j
+        sa = __funnelshift_l(__float_as_uint(v.x), sa, 4);
+        sb = __funnelshift_l(__float_as_uint(v.y), sb, 4);
       }
-      o.w[h] = wa - kSrPack;
-      o.w[h + 2] = wb - kSrPack;
+      o.w[h] = (wa - kSrPack) | (sa & 0x88888888u);
+      o.w[h + 2] = (wb - kSrPack) | (sb & 0x88888888u);
     }
   }
   if (emit_e4m3) {

@@ -125,6 +125,54 @@ def test_nv_given_amax_and_amax_pass(fq, orc):
         run_case(fq, orc, x, cfg, given=[float(g[0]) * 1.5, float(g[1]) * 0.5])   # caller's G (saturating too)
 
 
+def planted_sr_ties(orc, rows, cols, grid, seed, orient):
+    """Input whose stored copy ``orient`` (rows x cols in the copy's own
+    coordinates) has MX scale 1 in every block (element 0 of each block is the
+    block maximum 2^emax) and, wherever the draw r of an element's index has at
+    most 8 significant bits, an exact SR tie: |v| = (r / 2^16) g_1 on the lowest
+    interval [0, g_1), so that u = r / 2^16 equals the fraction and the element
+    rounds down.  The other elements are uniform in (-2^emax, 2^emax).  Returns
+    the bf16 input (transposed back for the column copy) and the tie mask."""
+    g = np.random.default_rng(seed)
+    top = np.float32(2.0 ** orc.grid_emax(grid))
+    g1 = np.float32(orc.grid_levels(grid)[1])
+    z = g.uniform(-1.0, 1.0, (rows, cols)).astype(np.float32) * top
+    ties = np.zeros((rows, cols), dtype=bool)
+    for i in range(rows):
+        for j in range(cols):
+            if j % 32 == 0:
+                z[i, j] = top if g.integers(2) else -top
+                continue
+            r = orc.sr_uniform16(seed, i * cols + j, orient)
+            if r and (r >> ((r & -r).bit_length() - 1)) < 256:
+                z[i, j] = np.float32(r) / np.float32(65536.0) * g1 * (1 if g.integers(2) else -1)
+                ties[i, j] = True
+    bits = synth.to_bf16_bits(z)
+    assert np.array_equal(synth.bf16_bits_to_f32(bits)[ties], z[ties])   # the ties are exact in bf16
+    return (bits if orient == 0 else np.ascontiguousarray(bits.T)), ties
+
+
+@pytest.mark.parametrize("grid", [0, 1, 2])
+def test_sr_exact_ties_round_down(fq, orc, grid):
+    """SR decides u < f strictly: an element whose fraction f equals its draw
+    u = r / 2^16 rounds down, on both copies (each copy draws from its own
+    index and orientation)."""
+    rows, cols = 64, 256
+    for orient in (0, 1):
+        seed = 4242 + 10 * grid + orient
+        x, ties = planted_sr_ties(orc, rows, cols, grid, seed, orient)
+        assert ties.sum() > 150
+        cfg = fq.Config(grid=grid, scale=0, rot=0, round=1, sr_seed=seed, want_row=(orient == 0),
+                        want_col=(orient == 1))
+        _, _, refs = run_case(fq, orc, x, cfg)
+        ref = refs[orient]
+        assert np.all(ref["scales"] == 127)
+        lo = ref["codes"] & 0xF
+        hi = ref["codes"] >> 4
+        codes = np.stack([lo, hi], axis=-1).reshape(rows, cols)
+        assert np.all((codes[ties] & 7) == 0)
+
+
 def top_of_range_input(top_exp: int) -> np.ndarray:
     """Rows 0-31: equal-sign 2^top_exp (1 + k/8); rows 32-47: normals times
     2^100..2^(top_exp - 3); row 48: half 2^(top_exp - 1), half 1e-38."""
