@@ -78,6 +78,34 @@ def test_gemm_small(fq, orc, grid, scale, M, N, K):
     check_gemm(fq, orc, a, b, grid, scale, 16, orc.sign_mask_from_seed(M * N, 16))
 
 
+@pytest.mark.parametrize("grid", [0, 1])
+@pytest.mark.parametrize("M,N,K", [(256, 640, 512), (384, 896, 256), (256, 4096, 1024)])
+def test_gemm_exact_tile_edges(fq, orc, grid, M, N, K):
+    """Grid-valued operands (unit MX scales, synth.grid_valued) make D = A B^T
+    exact in fp32, so the fp32 output equals the oracle's bit for bit and the
+    bf16 output is its rounding: every element of every tile, in both row
+    groups of the pair and in the 128-column tails of N = 640 and 896
+    (kind::mxf4 for E2M1, mxf8f6f4 for E1M2)."""
+    a = synth.grid_valued(M, K, 5 * M + K + grid, grid)
+    b = synth.grid_valued(N, K, 7 * N + K + grid, grid)
+    cfg = fq.Config(grid=grid, rot=0, want_col=False, sf_layout=fq.SF_MMA, emit_e4m3=(grid == fq.GRID_E1M2))
+    A, _ = fq.rht_quantize(synth.as_torch(a).cuda(), cfg)
+    B, _ = fq.rht_quantize(synth.as_torch(b).cuda(), cfg)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Dh, Df = fq.gemm(A, B, grid, fq.SCALE_MX, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _, da = oracle_operand(orc, a, grid, 0, 0, 0)
+    _, db = oracle_operand(orc, b, grid, 0, 0, 0)
+    D = orc.gemm_ref(da, db)
+    D32 = D.astype(np.float32)
+    assert np.array_equal(D, D32.astype(np.float64))   # exact in fp32
+    got = Df.cpu().numpy()
+    bad = np.argwhere(got.view(np.uint32) != D32.view(np.uint32))
+    assert bad.size == 0, f"{len(bad)} fp32 entries differ, first at {bad[:4].tolist()}"
+    assert np.array_equal(bf16_bits(Dh), synth.to_bf16_bits(D32))
+
+
 def test_gemm_nv_partial_k_tiles(fq, orc):
     # K = 320: NV-style K tiles of 256 + 64 (one MMA in the last tile)
     a = synth.normal(128, 320, 1)
