@@ -844,53 +844,65 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
       } else {
         // Plain output through a 32-row x 32-byte swizzled box per warp, stored
         // by TMA: fp32 columns as they leave TMEM, the bf16 row slice once the
-        // accumulator is released.
+        // accumulator is released.  The accumulator is released as soon as the
+        // last load has landed in registers; that chunk is converted after.
         constexpr int ECOLS = KK::kEpiCols, UNITS = (int)BOXB / 16;   // 16-byte units per box row
         constexpr int FCOLS = (int)BOXB / 4, HCOLS = (int)BOXB / 2;   // columns of an fp32 / bf16 box
         constexpr int LCOLS = 64;                                     // columns per TMEM load
+        constexpr int NLOADS = ECOLS / LCOLS;
         static_assert(ECOLS % LCOLS == 0 && ECOLS / 2 >= 32, "epilogue columns");
         uint32_t h[ECOLS / 2];   // this warp's columns of the row as packed bf16
+        // alpha, the fp32 stores and the bf16 words of the chunk at column c0
+        auto consume = [&](int c0, uint32_t (&r)[LCOLS]) {
+          if constexpr (KIND == KIND_NVF4) {
 #pragma unroll
-        for (int j = 0; j < ECOLS / 2; ++j) h[j] = 0u;
+            for (int j = 0; j < LCOLS; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), alpha));
+          }
+          if (want_f32 && live) {
 #pragma unroll
-        for (int c0 = 0; c0 < ECOLS; c0 += LCOLS) {
-          if (cbase + c0 < ncols) {   // ncols is 128 or 256: a load never straddles the edge
-            uint32_t r[LCOLS];
-            tmem_ld64(lane_base + (uint32_t)(cbase + c0), r, h + (c0 > 0 ? c0 / 2 - 32 : 0));
-            if constexpr (KIND == KIND_NVF4) {
+            for (int hh = 0; hh < LCOLS / FCOLS; ++hh) {
+              if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+              __syncwarp();
 #pragma unroll
-              for (int j = 0; j < LCOLS; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), alpha));
-            }
-            if (want_f32 && live) {
-#pragma unroll
-              for (int hh = 0; hh < LCOLS / FCOLS; ++hh) {
-                if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                __syncwarp();
-#pragma unroll
-                for (int u = 0; u < UNITS; ++u)
-                  st_shared16(stg + row_off + 16u * ((uint32_t)u ^ swz),
-                              make_uint4(r[FCOLS * hh + 4 * u], r[FCOLS * hh + 4 * u + 1], r[FCOLS * hh + 4 * u + 2],
-                                         r[FCOLS * hh + 4 * u + 3]));
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) {
-                  tma_store_2d(mDf, n0 + cbase + c0 + FCOLS * hh, y, stg);
-                  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                }
+              for (int u = 0; u < UNITS; ++u)
+                st_shared16(stg + row_off + 16u * ((uint32_t)u ^ swz),
+                            make_uint4(r[FCOLS * hh + 4 * u], r[FCOLS * hh + 4 * u + 1], r[FCOLS * hh + 4 * u + 2],
+                                       r[FCOLS * hh + 4 * u + 3]));
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(mDf, n0 + cbase + c0 + FCOLS * hh, y, stg);
+                asm volatile("cp.async.bulk.commit_group;" ::: "memory");
               }
             }
-#pragma unroll
-            for (int j = 0; j < LCOLS / 2; ++j) {
-              const __nv_bfloat162 b2 =
-                  __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-              h[c0 / 2 + j] = *reinterpret_cast<const uint32_t*>(&b2);
-            }
           }
+#pragma unroll
+          for (int j = 0; j < LCOLS / 2; ++j) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+            h[c0 / 2 + j] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+        };
+        auto release = [&]() {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) cluster_arrive(lead_acc_empty);
+        };
+        // ncols is 128 or 256 and a warp's columns start at 0 or 128, so a
+        // warp loads all of its columns or none
+        if (cbase < ncols) {
+          const uint32_t zero[32] = {};
+          uint32_t r[LCOLS];
+#pragma unroll
+          for (int k = 0; k < NLOADS; ++k) {
+            tmem_ld64(lane_base + (uint32_t)(cbase + k * LCOLS), r, k > 0 ? h + (k * LCOLS / 2 - 32) : zero);
+            if (k + 1 < NLOADS) consume(k * LCOLS, r);
+          }
+          // accumulator read out: let the next tile's MMAs start, then convert the last chunk
+          release();
+          consume(ECOLS - LCOLS, r);
+        } else {
+          release();
         }
-        // accumulator consumed: let the next tile's MMAs start
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) cluster_arrive(lead_acc_empty);
         if (want_bf16 && live) {
 #pragma unroll
           for (int b = 0; b < ECOLS / HCOLS; ++b) {
