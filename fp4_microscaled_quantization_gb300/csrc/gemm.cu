@@ -518,6 +518,12 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
   tc_fence_before();
   cluster_sync();
   tc_fence_after();
+  // Launched as a programmatic dependent of the stream's previous kernel: the
+  // setup above touched only this CTA's shared and tensor memory; wait for
+  // that grid to finish (its writes visible) before any global memory
+  // access, then let the next kernel's launch begin.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
   // barriers the leader owns, as seen from this CTA
   const uint32_t lead_full = mapa(bar_full, 0);
@@ -991,13 +997,17 @@ cudaError_t launch_pairs(Kern kern, int pairs, int smem, int threads, cudaStream
   cfg.blockDim = dim3((unsigned)threads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the kernel waits (griddepcontrol.wait)
+  // for the previous grid before touching global memory
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 

@@ -346,6 +346,11 @@ __device__ __forceinline__ void emit_chunk(float2 (&P)[16], const QuantParams& p
 template <int GRID, int SCALE, int NH, int ROUND>
 __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
     rht_quant_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
+  // Launched as a programmatic dependent of the stream's previous kernel:
+  // wait for that grid to finish (its writes visible) before any global
+  // memory access, then let the next kernel's launch begin.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr float kDen = 448.0f * GridK<GRID>::kQmax;
   constexpr int B = SCALE == FP4Q_SCALE_MX ? 32 : 16;
   float S_row = 0.0f, S_col = 0.0f;
@@ -623,14 +628,32 @@ static cudaError_t smem_attr(K kernel, bool& done, int smem = kQuantSmem) {
   return e;
 }
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the stream's previous kernel finishes; it waits for that grid
+// (griddepcontrol.wait) before touching global memory.
+template <class K, class... Args>
+static cudaError_t launch_dependent(K kernel, unsigned grid, int threads, int smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <int GRID, int SCALE, int NH, int ROUND>
 static cudaError_t launch_quant_inst(const CUtensorMap& m, const QuantParams& p, cudaStream_t s) {
   static bool attr = false;
   constexpr int smem = ring_smem(quant_stages<ROUND>());
   cudaError_t e = smem_attr(rht_quant_kernel<GRID, SCALE, NH, ROUND>, attr, smem);
   if (e != cudaSuccess) return e;
-  rht_quant_kernel<GRID, SCALE, NH, ROUND><<<persistent_grid(p, quant_ctas<ROUND>()), kNT, smem, s>>>(m, p);
-  return cudaGetLastError();
+  return launch_dependent(rht_quant_kernel<GRID, SCALE, NH, ROUND>, persistent_grid(p, quant_ctas<ROUND>()), kNT,
+                          smem, s, m, p);
 }
 
 template <int GRID, int SCALE, int NH>
