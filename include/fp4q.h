@@ -15,7 +15,11 @@
  *    never allocates, frees or keeps device memory; scratch comes from the
  *    caller's workspace argument.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
- *    asynchronous on it; nothing is synchronised unless stated.
+ *    asynchronous on it; nothing is synchronised unless stated.  The quantizer
+ *    and GEMM kernels launch as programmatic dependents of the stream's
+ *    previous kernel (their launch and on-chip setup may overlap its tail);
+ *    each waits for that kernel to complete before touching global memory,
+ *    so stream order holds as for any launch.
  *  - Arguments are validated before any launch.  A rejected call returns a
  *    non-zero fp4q_status and launches nothing.  A launch failure returns
  *    FP4Q_ERR_CUDA.
