@@ -37,16 +37,16 @@
 //               this CTA); every writer copies its rows of the chunks into the
 //               stage's TMEM scale slot with tcgen05.st and arrives on the
 //               stage's barrier in the leader.
-//   epilogue    (warps 2-5 and 10-13; 2-5 when the kernel quantizes its
-//               output) TMEM -> registers (tcgen05.ld, 64 columns a load in
-//               the plain kernels), alpha, fp32 / bf16, the accumulator is
-//               released to the next tile's MMAs (the one accumulator is
-//               single-buffered: the next tile's MMAs wait for it), then
-//               the stores by TMA: through 32-row x 32-byte boxes staged in
-//               1 KB per warp in the plain kernels; through a 128-byte
-//               swizzled 32 x 256 slice per warp in the kernels that quantize
-//               their output (TMA store, then the row-wise quantization of the
-//               slice).
+//   epilogue    (warps 2-5: columns 0-127, 10-13: columns 128-255) TMEM ->
+//               registers (tcgen05.ld, 64 columns a load in the plain
+//               kernels), alpha, fp32 / bf16, the accumulator is released to
+//               the next tile's MMAs as soon as the last load has landed (the
+//               one accumulator is single-buffered: the next tile's MMAs wait
+//               for it), then the stores by TMA: through 32-row x 32-byte
+//               boxes staged in 1 KB per warp in the plain kernels; through a
+//               128-byte swizzled 32 x 128 slice per warp in the kernels that
+//               quantize their output (TMA store, then the row-wise
+//               quantization of the slice).
 // Signals between the two CTAs are relaxed cluster-scope mbarrier arrivals:
 // what they announce is already complete when they are sent (TMEM writes
 // waited for with tcgen05.wait::st, TMEM reads with tcgen05.wait::ld), and a
@@ -133,17 +133,17 @@ struct KindK {
   // every stage has its TMEM scale slot beside the accumulator
   static constexpr int kStagesTmem = (int)(TMEM_COLS - 256) / kSfCols;
   // threads: producer, MMA, scale-writer warps, the epilogue warps (8, two
-  // per TMEM lane quarter; 4 in the kernels that quantize their output) and
-  // the scale-chunk loader (the last warp)
-  static constexpr int kEpiWarps = FUSED ? 4 : 8;
+  // per TMEM lane quarter, each with half of the tile's columns) and the
+  // scale-chunk loader (the last warp)
+  static constexpr int kEpiWarps = 8;
   static constexpr int kThreads = 32 * (7 + kEpiWarps);
   static constexpr int kChunkWarp = 6 + kEpiWarps;
   static constexpr int kEpiCols = 256 / (kEpiWarps / 4);   // accumulator columns per epilogue warp
   // shared-memory staging of an epilogue warp: one 32-row x 32-byte store box
-  // (plain kernels), or the warp's whole 32 x 256 bf16 slice of the tile
+  // (plain kernels), or the warp's whole 32 x 128 bf16 slice of the tile
   // (fused output quantization)
   static constexpr int kBoxBytes = FUSED ? 128 : 32;
-  static constexpr int kStgWarp = FUSED ? 16384 : 32 * kBoxBytes;
+  static constexpr int kStgWarp = FUSED ? 32 * 2 * kEpiCols : 32 * kBoxBytes;
   static constexpr int kFixed = kEpiWarps * kStgWarp + kBarBytes + 1024;
   static constexpr int kStagesFit = (kSmemMax - kFixed) / kSlot;
   static constexpr int kStagesCap = kStagesFit > kStagesTmem ? kStagesTmem : kStagesFit;
@@ -778,8 +778,8 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
       tc_fence_after();
       const int ncols = min(BN, t.N - n0);   // 128 or 256
       if constexpr (FUSED) {
-        // Fused output quantization.  The warp's 32 x 256 bf16 slice goes to
-        // shared memory as four swizzled 32 x 64 boxes (the previous tile's
+        // Fused output quantization.  The warp's 32 x 128 bf16 slice goes to
+        // shared memory as two swizzled 32 x 64 boxes (the previous tile's
         // stores must have read them), the accumulator is released, the boxes
         // are stored by TMA when D is wanted, and each thread quantizes its
         // row from them, 32 values at a time.  Box rows are 128 bytes: 16-byte
@@ -787,10 +787,10 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
         if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
         __syncwarp();
 #pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          if (c0 < ncols) {
+        for (int c0 = 0; c0 < KK::kEpiCols; c0 += 32) {
+          if (cbase + c0 < ncols) {
             uint32_t r[32];
-            tmem_ld32(lane_base + (uint32_t)c0, r);
+            tmem_ld32(lane_base + (uint32_t)(cbase + c0), r);
             uint32_t hw[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -817,13 +817,14 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
           if (lane == 0) {
-            for (int b = 0; 64 * b < ncols; ++b) tma_store_2d(&tmDh, n0 + 64 * b, y, stg + 4096u * (uint32_t)b);
+            for (int b = 0; 64 * b < KK::kEpiCols && cbase + 64 * b < ncols; ++b)
+              tma_store_2d(&tmDh, n0 + cbase + 64 * b, y, stg + 4096u * (uint32_t)b);
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
           }
         }
         const int64_t row = (int64_t)y + lane;
 #pragma unroll 1
-        for (int c0 = 0; c0 < ncols; c0 += 32) {
+        for (int c0 = 0; c0 < KK::kEpiCols && cbase + c0 < ncols; c0 += 32) {
           const uint32_t box = stg + 4096u * (uint32_t)(c0 / 64), u0 = 4u * (uint32_t)((c0 / 32) & 1);
           uint32_t wq[16];
 #pragma unroll
@@ -834,7 +835,7 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
           if (p.q_nh == 16) rotate_chunk<16, false>(P);
           else if (p.q_nh == 32) rotate_chunk<32>(P);
           ChunkOut o;
-          const int64_t col = (int64_t)n0 + c0;
+          const int64_t col = (int64_t)n0 + cbase + c0;
           quantize_chunk<(QG >= 0 ? QG : 0), FP4Q_SCALE_MX, QR>(P, 0.0f, (uint64_t)(row * p.N + col), 0u, p.q_keys,
                                                                  p.q_e4m3 != nullptr, p.status, o,
                                                                  p.q_nh == 16 ? 2 : 0);
