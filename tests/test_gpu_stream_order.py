@@ -65,3 +65,41 @@ def test_overwrite_gemm_requantize_chain(fq, orc):
     qy = orc.quantize(d_bits, 0, 1, 0, 16, 0x0F0F, 1, 31)
     assert np.array_equal(Yq.codes.cpu().numpy(), qy["codes"])
     assert np.array_equal(Yq.scales.cpu().numpy(), qy["scales"])
+
+
+def test_cuda_graph_capture_and_replay(fq):
+    """The quantizer and GEMM launches (programmatic dependents, no host
+    synchronisation or allocation inside a call) can be captured in a CUDA
+    graph; a replay on new inputs gives the bits an eager run gives."""
+    M, N, K = 256, 384, 512
+    cfg = fq.Config(grid=0, rot=16, sign_mask_row=0x2468, want_col=False, sf_layout=fq.SF_MMA)
+    X = synth.as_torch(synth.normal(M, K, 21)).cuda()
+    W = synth.as_torch(synth.normal(N, K, 22, 0.05)).cuda()
+    Xr, _ = fq.rht_quantize(X, cfg)
+    Wr, _ = fq.rht_quantize(W, cfg)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):   # warm-up outside the capture
+        fq.rht_quantize(X, cfg, Xr, status=st)
+        fq.gemm(Xr, Wr, 0, fq.SCALE_MX, want_f32=False, D_bf16=D, status=st)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fq.rht_quantize(X, cfg, Xr, status=st)
+        fq.rht_quantize(W, cfg, Wr, status=st)
+        fq.gemm(Xr, Wr, 0, fq.SCALE_MX, want_f32=False, D_bf16=D, status=st)
+    X.copy_(synth.as_torch(synth.normal_point_outliers(M, K, 23)).cuda())
+    W.copy_(synth.as_torch(synth.normal(N, K, 24, 0.05)).cuda())
+    graph.replay()
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    got = (Xr.codes.clone(), Wr.codes.clone(), D.clone())
+    Xe, _ = fq.rht_quantize(X, cfg)
+    We, _ = fq.rht_quantize(W, cfg)
+    De, _ = fq.gemm(Xe, We, 0, fq.SCALE_MX, want_f32=False)
+    torch.cuda.synchronize()
+    assert torch.equal(got[0], Xe.codes) and torch.equal(got[1], We.codes)
+    assert torch.equal(got[2], De)
