@@ -162,6 +162,7 @@ extern "C" {
 int32_t fp4q_rht_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, const fp4q_config* cfg,
                           const fp4q_operand* row_out, const fp4q_operand* col_out, void* workspace,
                           size_t ws_bytes, uint32_t* d_status, void* stream) {
+  fp4q::NvtxRange nvtx_range("fp4q_rht_quantize");
   return rht_quantize_impl(x, rows, cols, ld, cfg, row_out, col_out, workspace, ws_bytes, d_status, stream, -1, 0);
 }
 
@@ -170,6 +171,7 @@ int32_t fp4q_test_quantize_wait_expiry(const void* x, int64_t rows, int64_t cols
                                        const fp4q_operand* col_out, void* workspace, size_t ws_bytes,
                                        uint32_t* d_status, int32_t stall_tile, uint32_t wait_limit_us,
                                        void* stream) {
+  fp4q::NvtxRange nvtx_range("fp4q_test_quantize_wait_expiry");
   if (stall_tile < 0 || wait_limit_us == 0 || wait_limit_us > 2000000u) return FP4Q_ERR_INVALID_ARG;
   return rht_quantize_impl(x, rows, cols, ld, cfg, row_out, col_out, workspace, ws_bytes, d_status, stream,
                            stall_tile, wait_limit_us * 1000u);
@@ -177,6 +179,7 @@ int32_t fp4q_test_quantize_wait_expiry(const void* x, int64_t rows, int64_t cols
 
 int32_t fp4q_rotated_amax(const void* x, int64_t rows, int64_t cols, int64_t ld, const fp4q_config* cfg,
                           float* amax_out, uint32_t* d_status, void* stream) {
+  fp4q::NvtxRange nvtx_range("fp4q_rotated_amax");
   QuantParams p;
   int32_t st = prepare(x, rows, cols, ld, cfg, p);
   if (st != FP4Q_OK) return st;
@@ -190,6 +193,7 @@ int32_t fp4q_rotated_amax(const void* x, int64_t rows, int64_t cols, int64_t ld,
 
 int32_t fp4q_dequantize(const fp4q_operand* q, int64_t rows, int64_t cols, const fp4q_config* cfg,
                         int32_t orient, int32_t unrotate, float* out, void* stream) {
+  fp4q::NvtxRange nvtx_range("fp4q_dequantize");
   if (!valid_cfg(cfg) || !q || (orient != 0 && orient != 1)) return FP4Q_ERR_INVALID_ARG;
   if (rows < 0 || cols < 0) return FP4Q_ERR_INVALID_ARG;
   if (rows == 0 || cols == 0) return FP4Q_OK;
@@ -214,6 +218,7 @@ size_t fp4q_bias_stats_workspace_bytes(int64_t n) { return bias_stats_workspace(
 
 int32_t fp4q_bias_stats(const float* ref, const float* approx, int64_t n, const uint8_t* codes,
                         void* workspace, size_t ws_bytes, void* out, void* stream) {
+  fp4q::NvtxRange nvtx_range("fp4q_bias_stats");
   if (n < 0 || !out) return FP4Q_ERR_INVALID_ARG;
   if (n > 0 && (!ref || !approx)) return FP4Q_ERR_INVALID_ARG;
   if (codes && (n % 2 != 0)) return FP4Q_ERR_INVALID_ARG;
@@ -240,6 +245,7 @@ void fp4q_stats_finalize(const double* s, double* sqnr_db, double* alpha, double
 int32_t fp4q_hadamard_rotate_bf16(const void* x, int64_t rows, int64_t cols, int64_t ld, int32_t rot,
                                   uint32_t sign_mask_row, uint32_t sign_mask_col, void* y_row, void* y_col,
                                   void* stream) {
+  fp4q::NvtxRange nvtx_range("fp4q_hadamard_rotate_bf16");
   if (rot != FP4Q_ROT_H16 && rot != FP4Q_ROT_H32) return FP4Q_ERR_INVALID_ARG;
   if (!y_row && !y_col) return FP4Q_ERR_INVALID_ARG;
   fp4q_config c;

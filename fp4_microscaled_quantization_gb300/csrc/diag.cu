@@ -215,6 +215,7 @@ extern "C" size_t fp4q_diag_workspace_bytes(void) { return fp4q::diag_workspace(
 extern "C" int32_t fp4q_grid_error(const void* x, int64_t rows, int64_t cols, int64_t ld, const fp4q_config* cfg,
                                    const fp4q_operand* row_copy, void* workspace, size_t ws_bytes, void* out,
                                    void* stream) {
+  fp4q::NvtxRange nvtx_range("fp4q_grid_error");
   using namespace fp4q;
   if (!cfg || !row_copy || !out || !x) return FP4Q_ERR_INVALID_ARG;
   if (cfg->grid != FP4Q_GRID_E2M1 && cfg->grid != FP4Q_GRID_E1M2 && cfg->grid != FP4Q_GRID_E2M1_R4)
@@ -260,6 +261,7 @@ extern "C" int32_t fp4q_grid_error(const void* x, int64_t rows, int64_t cols, in
 
 extern "C" int32_t fp4q_rel_error(const float* ref, const float* approx, int64_t n, void* workspace,
                                   size_t ws_bytes, void* out, void* stream) {
+  fp4q::NvtxRange nvtx_range("fp4q_rel_error");
   using namespace fp4q;
   if (n < 0 || !out) return FP4Q_ERR_INVALID_ARG;
   if (n > 0 && (!ref || !approx)) return FP4Q_ERR_INVALID_ARG;

@@ -4,9 +4,19 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 namespace fp4q {
+
+// NVTX range over one C-ABI call: named in profiler timelines (ncu can filter
+// launches by it), a no-op when no profiler is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // One output copy of the quantizer (device pointers).
 struct CopyOut {

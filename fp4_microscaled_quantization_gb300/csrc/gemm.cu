@@ -1178,6 +1178,7 @@ cudaError_t launch_kind(int kind, const CUtensorMap& ta, const CUtensorMap& tb, 
 extern "C" int32_t fp4q_gemm(const fp4q_operand* A, const fp4q_operand* B, int64_t M, int64_t N, int64_t K,
                              int32_t grid, int32_t scale, void* D_bf16, float* D_f32, uint32_t* d_status,
                              void* stream) {
+  fp4q::NvtxRange nvtx_range("fp4q_gemm");
   using namespace fp4q;
   if (!D_bf16 && !D_f32) return FP4Q_ERR_INVALID_ARG;
   int kind = 0;
@@ -1192,6 +1193,7 @@ extern "C" int32_t fp4q_gemm(const fp4q_operand* A, const fp4q_operand* B, int64
 
 extern "C" int32_t fp4q_gemm_group(const fp4q_gemm_problem* problems, int32_t count, int32_t grid, int32_t scale,
                                    uint32_t* d_status, void* stream) {
+  fp4q::NvtxRange nvtx_range("fp4q_gemm_group");
   using namespace fp4q;
   if (!problems || count < 1 || count > kGroupMax) return FP4Q_ERR_INVALID_ARG;
   static thread_local GroupArgs ga;   // ~19 KB: copied into the launch, reused by the next call
@@ -1232,6 +1234,7 @@ extern "C" int32_t fp4q_gemm_group(const fp4q_gemm_problem* problems, int32_t co
 extern "C" int32_t fp4q_gemm_quantize(const fp4q_operand* A, const fp4q_operand* B, int64_t M, int64_t N, int64_t K,
                                       int32_t grid, int32_t scale, void* D_bf16, const fp4q_config* out_cfg,
                                       fp4q_operand* out, uint32_t* d_status, void* stream) {
+  fp4q::NvtxRange nvtx_range("fp4q_gemm_quantize");
   using namespace fp4q;
   if (!out_cfg || !out || !out->codes || !out->scales) return FP4Q_ERR_INVALID_ARG;
   const fp4q_config& c = *out_cfg;

@@ -158,6 +158,7 @@ extern "C" void fp4q_bias_stats_noalloc_reset(void) {
 
 extern "C" int32_t fp4q_bias_stats_noalloc(const float* ref, const float* approx, int64_t n,
                                            const uint8_t* codes, void* out, void* stream) {
+  fp4q::NvtxRange nvtx_range("fp4q_bias_stats_noalloc");
   using namespace fp4q;
   if (n < 0 || !out) return FP4Q_ERR_INVALID_ARG;
   if (n > 0 && (!ref || !approx)) return FP4Q_ERR_INVALID_ARG;

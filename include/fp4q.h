@@ -20,6 +20,9 @@
  *    previous kernel (their launch and on-chip setup may overlap its tail);
  *    each waits for that kernel to complete before touching global memory,
  *    so stream order holds as for any launch.
+ *  - Every call that launches work is an NVTX range named after the entry
+ *    point (for profiler timelines and `ncu --nvtx` filters; a no-op when no
+ *    profiler is attached).
  *  - Arguments are validated before any launch.  A rejected call returns a
  *    non-zero fp4q_status and launches nothing.  A launch failure returns
  *    FP4Q_ERR_CUDA.
