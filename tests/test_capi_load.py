@@ -83,6 +83,7 @@ def test_validation_rejects_before_launch(fq):
     assert _quant(fq, fake, 64, 64, 64, fq.Config(want_row=False, want_col=False)) == fq.ERR_INVALID_ARG
     assert _quant(fq, fake, 64, 64, 64, cfg, None, op) == fq.ERR_INVALID_ARG          # missing row copy
     assert _quant(fq, fake, 64, 64, 64, fq.Config(sf_layout=fq.SF_MMA), op, op) == fq.ERR_INVALID_ARG  # rows % 128
+    assert _quant(fq, fake, 65535 * 64 + 32, 64, 64, cfg, op, op) == fq.ERR_INVALID_ARG  # (rows + 63) / 64 > 65535
     assert _quant(fq, fake, 128, 128, 128, fq.Config(scale=fq.SCALE_NV), op, op) == fq.ERR_WORKSPACE
     nots = fq.COperand(fake, fake, None, None)
     assert _quant(fq, fake, 128, 128, 128, fq.Config(scale=fq.SCALE_NV), nots, nots) == fq.ERR_INVALID_ARG
@@ -91,3 +92,7 @@ def test_validation_rejects_before_launch(fq):
     assert L.fp4q_bias_stats(fake, fake, 100, None, None, 0, fake, None) == fq.ERR_WORKSPACE
     assert L.fp4q_bias_stats(fake, fake, 101, fake, fake, 1 << 30, fake, None) == fq.ERR_INVALID_ARG
     assert L.fp4q_hadamard_rotate_bf16(fake, 64, 64, 64, 0, 0, 0, fake, None, None) == fq.ERR_INVALID_ARG
+    # GEMM shape limits: M / 128 <= 65535, N and K <= INT32_MAX
+    for M, N, K in ((65536 * 128, 128, 128), (128, 1 << 31, 128), (128, 128, 1 << 31)):
+        assert L.fp4q_gemm(ctypes.byref(op), ctypes.byref(op), M, N, K, 0, 0, fake, None, None,
+                           None) == fq.ERR_INVALID_ARG

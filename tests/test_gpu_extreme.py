@@ -45,7 +45,8 @@ def check_col_groups(orc, bits, cfg, co, r0s):
         assert np.array_equal(scales[:, r0 // b:(r0 + 32) // b], want["scales"]), f"rows {r0}.. scales"
 
 
-@pytest.mark.parametrize("R,C", [(64, 1 << 19), (1 << 20, 32)])
+# the last shape is the most rows the quantizer accepts, (rows + 63) / 64 = 65535
+@pytest.mark.parametrize("R,C", [(64, 1 << 19), (1 << 20, 32), (65535 * 64, 32)])
 def test_quantizer_wide_and_tall(fq, orc, R, C):
     bits = synth.normal_point_outliers(R, C, R + C, 0.001, 40.0)
     cfg = fq.Config(rot=16, sign_mask_row=0x2D4B, sign_mask_col=0x8E31)
@@ -58,6 +59,48 @@ def test_quantizer_wide_and_tall(fq, orc, R, C):
     check_rows(orc, bits, cfg, ro, sorted({0, R - 1, *rng.integers(0, R, 6).tolist()}))
     groups = sorted({0, (R - 32) // 32 * 32, *(rng.integers(0, R // 32, 6) * 32).tolist()})
     check_col_groups(orc, bits, cfg, co, groups)
+
+
+def mma_layout(plain):
+    """Scale bytes [rows, nkb] placed in the MMA scale layout (512-byte groups
+    of 128 rows by four K-blocks)."""
+    rows, nkb = plain.shape
+    r = np.arange(rows)[:, None]
+    k = np.arange(nkb)[None, :]
+    off = ((r // 128) * (nkb // 4) + k // 4) * 512 + 16 * (r % 32) + 4 * ((r // 32) % 4) + k % 4
+    out = np.empty(rows * nkb, dtype=np.uint8)
+    out[off.reshape(-1)] = plain.reshape(-1)
+    return out.reshape(rows, nkb)
+
+
+def test_gemm_maximum_m(fq, orc):
+    """The largest M the GEMM accepts (M / 128 = 65535, so its last 256-row
+    tile is a 128-row tail) on sampled entries against the oracle.  A is made
+    of seeded random E2M1 code bytes and E8M0 scale bytes 2^-7 .. 2^7 (the
+    quantizer takes at most 65535 * 64 rows in one call)."""
+    M, N, K = 65535 * 128, 128, 128
+    rng = np.random.default_rng(65535)
+    a_codes = rng.integers(0, 256, (M, K // 2), dtype=np.uint8)
+    a_scales = rng.integers(120, 135, (M, K // 32), dtype=np.uint8)
+    A = fq.Operand(codes=torch.from_numpy(a_codes).cuda(), scales=torch.from_numpy(mma_layout(a_scales)).cuda(),
+                   rows=M, cols=K, sf_layout=fq.SF_MMA)
+    b = synth.normal(N, K, 77, 0.05)
+    cfg = fq.Config(rot=16, sign_mask_row=0x3C5A, want_col=False, sf_layout=fq.SF_MMA)
+    B, _ = fq.rht_quantize(synth.as_torch(b).cuda(), cfg)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _, D = fq.gemm(A, B, 0, 0, want_bf16=False, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    ii = np.concatenate([[0, 127, M - 256, M - 129, M - 128, M - 1], rng.integers(0, M, 250)])
+    jj = rng.integers(0, N, ii.size)
+    rows_a = np.unique(ii)
+    da = orc.dequantize(np.ascontiguousarray(a_codes[rows_a]), np.ascontiguousarray(a_scales[rows_a]), 0, 0, 0)
+    qb = orc.quantize(b, 0, 0, 0, 16, cfg.sign_mask_row)
+    db = orc.dequantize(qb["codes"], qb["scales"], 0, 0, 0)
+    want = orc.gemm_entries(da, db, np.searchsorted(rows_a, ii), jj)
+    got = D[torch.from_numpy(ii).cuda(), torch.from_numpy(jj).cuda()].double().cpu().numpy()
+    rel = np.linalg.norm(got - want) / np.linalg.norm(want)
+    assert rel <= 1e-3, f"sampled relative Frobenius error {rel:.3e}"
 
 
 @pytest.mark.parametrize("M,N,K", [(1 << 17, 128, 128), (128, 1 << 16, 256), (256, 256, 1 << 16)])
