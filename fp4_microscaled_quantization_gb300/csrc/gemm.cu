@@ -508,6 +508,16 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // the operand maps are kernel parameters: fetch them before the wait below
+    if constexpr (GROUP) {
+      for (int q = 0; q < ga.np; ++q) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&ga.a[q]) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(&ga.b[q]) : "memory");
+      }
+    } else {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
+    }
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -532,15 +542,6 @@ __global__ void __launch_bounds__(KindK<KIND, (QG >= 0)>::kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- operand producer
-      if constexpr (GROUP) {
-        for (int q = 0; q < ga.np; ++q) {
-          asm volatile("prefetch.tensormap [%0];" ::"l"(&ga.a[q]) : "memory");
-          asm volatile("prefetch.tensormap [%0];" ::"l"(&ga.b[q]) : "memory");
-        }
-      } else {
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
-      }
       uint32_t it = 0;
       bool ok = true;
       for (int w = w_begin; w < w_end && ok; w += w_step) {

@@ -151,8 +151,10 @@ struct TileRing {
           : "memory");
   }
 
-  __device__ __forceinline__ void init(const CUtensorMap* tmap, int64_t rows, int64_t cols,
-                                      int stall = -1, uint32_t stall_ns = 0) {
+  // The ring's barriers and the tensor map's prefetch: no global data is
+  // touched, so a programmatic dependent may run this before its wait.
+  __device__ __forceinline__ void setup(const CUtensorMap* tmap, int64_t rows, int64_t cols,
+                                       int stall = -1, uint32_t stall_ns = 0) {
     extern __shared__ uint8_t smem_raw[];
     smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     bar0 = smem_addr(smem + kStages * kTileBytes);
@@ -166,15 +168,23 @@ struct TileRing {
       for (int s = 0; s <= kStages; ++s)
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar0 + 8 * s) : "memory");
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
     }
     __syncthreads();
+  }
+  // The first kStages loads.
+  __device__ __forceinline__ void start() const {
     if (threadIdx.x == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
       for (int s = 0; s < kStages; ++s) {
         const int t = blockIdx.x + s * gridDim.x;
         if (t < ntiles) issue(s, t);
       }
     }
+  }
+  __device__ __forceinline__ void init(const CUtensorMap* tmap, int64_t rows, int64_t cols,
+                                      int stall = -1, uint32_t stall_ns = 0) {
+    setup(tmap, rows, cols, stall, stall_ns);
+    start();
   }
 
   __device__ __forceinline__ TileView view(int k) const { return TileView{smem + (k % kStages) * kTileBytes}; }
@@ -346,11 +356,15 @@ __device__ __forceinline__ void emit_chunk(float2 (&P)[16], const QuantParams& p
 template <int GRID, int SCALE, int NH, int ROUND>
 __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
     rht_quant_kernel(const __grid_constant__ CUtensorMap tmx, const QuantParams p) {
-  // Launched as a programmatic dependent of the stream's previous kernel:
+  // Launched as a programmatic dependent of the stream's previous kernel: the
+  // ring's setup touches only shared memory and the kernel parameters; then
   // wait for that grid to finish (its writes visible) before any global
-  // memory access, then let the next kernel's launch begin.
+  // memory access, and let the next kernel's launch begin.
+  TileRing<quant_stages<ROUND>()> ring;
+  ring.setup(&tmx, p.rows, p.cols, p.stall_tile, p.wait_limit_ns);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  ring.start();
   constexpr float kDen = 448.0f * GridK<GRID>::kQmax;
   constexpr int B = SCALE == FP4Q_SCALE_MX ? 32 : 16;
   float S_row = 0.0f, S_col = 0.0f;
@@ -362,8 +376,6 @@ __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
       if (p.want_col) *p.col.tensor_scale = S_col;
     }
   }
-  TileRing<quant_stages<ROUND>()> ring;
-  ring.init(&tmx, p.rows, p.cols, p.stall_tile, p.wait_limit_ns);
 
   // ---- offsets of this thread's chunks that do not change from tile to tile
   const int tid = threadIdx.x;
