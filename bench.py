@@ -348,10 +348,9 @@ def run_ours(args, world, rank, local):
             ncu_peak = 49152 * n_sm * sm_max_mhz * 1e6 / 1e12
             out["ncu_fp4_peak"] = round(ncu_peak, 1)
             out["frac_of_ncu_fp4_peak"] = round(achieved / ncu_peak, 4)
-            g_traffic = traffic.get("gemm_mxf4_fprop_bytes"), traffic.get("gemm_mxf4_group_dgrad_wgrad_bytes")
-            out["traffic"] = (g_traffic[0] + g_traffic[1]) // 2 if all(g_traffic) else None
-        else:
-            out["traffic"] = None
+        key = "gemm_mxf4" if r == "e2m1" else "gemm_mxf8f6f4"
+        g_traffic = traffic.get(f"{key}_fprop_bytes"), traffic.get(f"{key}_group_dgrad_wgrad_bytes")
+        out["traffic"] = (g_traffic[0] + g_traffic[1]) // 2 if all(g_traffic) else None
         out["traffic_source"] = "ncu capture summarised in profiles/dram_traffic.txt (per launch, mean of the two)"
         return out
 
