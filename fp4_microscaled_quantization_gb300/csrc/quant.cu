@@ -334,7 +334,17 @@ __device__ __forceinline__ void emit_chunk(float2 (&P)[16], const QuantParams& p
                                            int64_t e4_off) {
   constexpr bool kMX = SCALE == FP4Q_SCALE_MX;
   ChunkOut o;
-  if constexpr (kMX) {
+  if constexpr (kMX && ROUND == FP4Q_SR) {
+    // the chunk's random words first: their chains overlap the rotation's
+    Philox4 R[4];
+    const uint64_t c = idx0 >> 3;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      R[q] = philox4x32_10_rk((uint32_t)(c + q), (uint32_t)((c + q) >> 32), orient, 0u, p.sr_keys);
+    const float m = rotate_chunk_mx<NH>(P);
+    quantize_chunk<GRID, SCALE, ROUND, true>(P, S_t, idx0, orient, p.sr_keys, p.emit_e4m3, p.status, o,
+                                             NH == 16 ? 2 : 0, m, R);
+  } else if constexpr (kMX) {
     // H16's 1/4 goes into the power-of-two block scale
     const float m = rotate_chunk_mx<NH>(P);
     quantize_chunk<GRID, SCALE, ROUND, true>(P, S_t, idx0, orient, p.sr_keys, p.emit_e4m3, p.status, o,

@@ -276,11 +276,14 @@ struct ChunkOut {
 //          with the same single rounding.
 //   GIVEN  MX only: m_given is the block maximum max |P| (rotate_chunk_mx)
 //          instead of a maximum taken here.
+//   R      SR only, optional: the chunk's four Philox results (counters
+//          idx0/8 + 0..3) computed by the caller, so that their dependency
+//          chains can overlap the rotation; null computes them here.
 template <int GRID, int SCALE, int ROUND, bool GIVEN = false>
 __device__ __forceinline__ void quantize_chunk(float2 (&P)[16], float S_t, uint64_t idx0,
                                                uint32_t orient, const uint32_t (&rk)[20],
                                                bool emit_e4m3, uint32_t* status, ChunkOut& o, int pre = 0,
-                                               float m_given = 0.0f) {
+                                               float m_given = 0.0f, const Philox4* R = nullptr) {
   constexpr float QMAX = GridK<GRID>::kQmax;
   static_assert(!GIVEN || SCALE == FP4Q_SCALE_MX, "a given maximum is an MX block maximum");
   // block amax (NaN-propagating) of each 16-lane half
@@ -389,8 +392,8 @@ __device__ __forceinline__ void quantize_chunk(float2 (&P)[16], float S_t, uint6
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint64_t ca = c + (uint64_t)h, cb = ca + 2u;
-      const Philox4 ra = philox4x32_10_rk((uint32_t)ca, (uint32_t)(ca >> 32), orient, 0u, rk);
-      const Philox4 rb = philox4x32_10_rk((uint32_t)cb, (uint32_t)(cb >> 32), orient, 0u, rk);
+      const Philox4 ra = R ? R[h] : philox4x32_10_rk((uint32_t)ca, (uint32_t)(ca >> 32), orient, 0u, rk);
+      const Philox4 rb = R ? R[h + 2] : philox4x32_10_rk((uint32_t)cb, (uint32_t)(cb >> 32), orient, 0u, rk);
       constexpr uint32_t kSrPack = kSrOff * 0x11111111u;
       uint32_t wa = 0, wb = 0, sa = 0, sb = 0;
 #pragma unroll
