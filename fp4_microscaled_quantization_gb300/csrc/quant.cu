@@ -314,11 +314,12 @@ __device__ __forceinline__ void read_row_chunk_sw(const TileView& tv, int r, int
 // two CTAs per SM; the other modes with three.
 template <int ROUND>
 constexpr int quant_ctas() { return ROUND == FP4Q_SR ? 2 : QUANT_MIN_CTAS; }
-// Tiles in flight per CTA, measured on the linear-layer tensors (X 16384 x
-// 4096 both copies, CUDA events, L2 flushed): RTNE 60.1 / 61.1 / 62.1 us with
-// 2 / 3 / 4 stages, SR 168.6 / 166.5 / 170.6 us.
-template <int ROUND>
-constexpr int quant_stages() { return ROUND == FP4Q_SR ? 3 : 2; }
+// Tiles in flight per CTA, measured on the linear-layer tensors (16384 x 4096
+// both copies, CUDA events, L2 flushed): RTNE 60.1 / 61.1 / 62.1 us with
+// 2 / 3 / 4 stages; SR on the E2M1 grid 133.8 / 131.7 / 133.8 us, on the E1M2
+// and capped E2M1 grids 137.9 / 139.9 / 140.0 us.
+template <int ROUND, int GRID>
+constexpr int quant_stages() { return ROUND == FP4Q_SR && GRID == FP4Q_GRID_E2M1 ? 3 : 2; }
 
 // Where one thread's chunks of a copy go: offsets that depend only on the
 // thread (fixed over the tiles) plus, per tile, the tile's own.
@@ -370,7 +371,7 @@ __global__ void __launch_bounds__(kNT, quant_ctas<ROUND>())
   // ring's setup touches only shared memory and the kernel parameters; then
   // wait for that grid to finish (its writes visible) before any global
   // memory access, and let the next kernel's launch begin.
-  TileRing<quant_stages<ROUND>()> ring;
+  TileRing<quant_stages<ROUND, GRID>()> ring;
   ring.setup(&tmx, p.rows, p.cols, p.stall_tile, p.wait_limit_ns);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -671,7 +672,7 @@ static cudaError_t launch_dependent(K kernel, unsigned grid, int threads, int sm
 template <int GRID, int SCALE, int NH, int ROUND>
 static cudaError_t launch_quant_inst(const CUtensorMap& m, const QuantParams& p, cudaStream_t s) {
   static bool attr = false;
-  constexpr int smem = ring_smem(quant_stages<ROUND>());
+  constexpr int smem = ring_smem(quant_stages<ROUND, GRID>());
   cudaError_t e = smem_attr(rht_quant_kernel<GRID, SCALE, NH, ROUND>, attr, smem);
   if (e != cudaSuccess) return e;
   return launch_dependent(rht_quant_kernel<GRID, SCALE, NH, ROUND>, persistent_grid(p, quant_ctas<ROUND>()), kNT,
